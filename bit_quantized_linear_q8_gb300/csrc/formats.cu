@@ -1,0 +1,322 @@
+// formats.cu -- weight packing, dequantisation, activation quantisation and SiLU*mul.
+//
+// All of these are HBM-bound streaming kernels: coalesced 8/16-byte accesses, grid sized
+// as a multiple of the SM count, no shared memory.
+#include "common.cuh"
+
+namespace bq8 {
+
+// =====================================================================================
+// Q2_0 pack: codes [n][k] (one per byte) + scales [n][k/group] -> packed buffer.
+// Thread -> 4 output bytes (l0..l0+3 of one 32-byte pack block): byte l of pack block p
+// holds the codes of columns 128p + 32i + l in bits 2i (i = 0..3).
+// Source: init_q2.rs, `set_packed_q2_qkvz` (the packed weight it installs).
+// =====================================================================================
+__global__ void q2_pack_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
+                               uint8_t* __restrict__ out, int64_t n, int64_t k, int64_t nsc) {
+    const int64_t words_per_row = k / 16;  // 4 output bytes per thread, k/4 bytes per row
+    const int64_t total = n * words_per_row;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t id = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; id < total; id += stride) {
+        const int64_t r = id / words_per_row, wi = id % words_per_row;
+        const int64_t p = wi / 8, l0 = (wi % 8) * 4;
+        const uint8_t* src = codes + r * k + p * 128 + l0;
+        uint32_t word = 0;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const uint32_t c4 = *reinterpret_cast<const uint32_t*>(src + 32 * i);
+            word |= (c4 & 0x03030303u) << (2 * i);
+        }
+        *reinterpret_cast<uint32_t*>(out + r * (k / 4) + p * 32 + l0) = word;
+    }
+    uint16_t* sc_out = reinterpret_cast<uint16_t*>(out + n * (k / 4));
+    for (int64_t id = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; id < nsc; id += stride) sc_out[id] = scales[id];
+}
+
+// =====================================================================================
+// Q2_0 -> BF16: w = d * (c - 2), exact.
+// Thread -> 8 packed bytes (32 codes) = 4 runs of 8 consecutive columns.  Each code is
+// moved into mantissa bits 5..6 of a bf16 1.0 (value 1 + c/4), then (v - 1.5) * 4d gives
+// d*(c-2) exactly (both steps are exact in BF16).
+// Source: init_q2.rs, `qkvz_q2_prefill_gemm` fallback (`dequant_q2_0_gn_to_bf16`).
+// =====================================================================================
+__global__ void __launch_bounds__(256) q2_dequant_kernel(const uint8_t* __restrict__ packed, uint16_t* __restrict__ out,
+                                                         int64_t n, int64_t k, int group) {
+    const int64_t q_per_row = k / 32;  // 8-byte quarters of pack blocks per row
+    const int64_t total = n * q_per_row;
+    const int64_t groups = k / group;
+    const uint16_t* sc = reinterpret_cast<const uint16_t*>(packed + n * (k / 4));
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const __nv_bfloat162 c15 = __floats2bfloat162_rn(1.5f, 1.5f);
+    for (int64_t id = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; id < total; id += stride) {
+        const int64_t r = id / q_per_row, qi = id % q_per_row;
+        const int64_t p = qi / 4, l0 = (qi % 4) * 8;
+        const uint2 w = ldg_stream64(packed + r * (k / 4) + p * 32 + l0);
+        const float d = bf16_bits_to_f32(sc[r * groups + (p * 128) / group]);
+        const __nv_bfloat162 d4 = __floats2bfloat162_rn(4.0f * d, 4.0f * d);
+        // bytes (b, b+1) into the low byte of each 16-bit half
+        const uint32_t e[4] = {__byte_perm(w.x, 0, 0x4140), __byte_perm(w.x, 0, 0x4342), __byte_perm(w.y, 0, 0x4140),
+                               __byte_perm(w.y, 0, 0x4342)};
+        uint16_t* dst = out + r * k + p * 128 + l0;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const uint32_t s = (i < 3) ? (e[j] << (5 - 2 * i)) : (e[j] >> 1);
+                const uint32_t v = (s & 0x00600060u) | 0x3F803F80u;
+                o[j] = bf162_bits(__hmul2(__hsub2(bits_bf162(v), c15), d4));
+            }
+            *reinterpret_cast<uint4*>(dst + 32 * i) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
+// =====================================================================================
+// q8_1 quantisation.  Thread -> 8 values; a quad of 4 threads owns one 32-value block.
+// d = amax/127, q = round-half-away(x/d), s = d*sum(q), every step an IEEE fp32
+// operation rounded to nearest (explicit _rn intrinsics, no contraction).
+// Source: q4k_mmq.rs, `quantize_act_q8_1`.
+// =====================================================================================
+template <bool VEC>
+__global__ void __launch_bounds__(256) q8_1_kernel(const uint16_t* __restrict__ x, int8_t* __restrict__ codes,
+                                                   float2* __restrict__ ds, int64_t m, int64_t k, int64_t kp) {
+    const int64_t per_row = kp / 8;
+    const int64_t total = m * per_row;  // multiple of 32: kp % 256 == 0
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t id = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; id < total; id += stride) {
+        const int64_t r = id / per_row, c0 = (id % per_row) * 8;
+        float v[8];
+        if (VEC && c0 + 8 <= k) {
+            const uint4 u = *reinterpret_cast<const uint4*>(x + r * k + c0);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                v[2 * j] = __uint_as_float(w[j] << 16);
+                v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; j++) v[j] = (c0 + j < k) ? bf16_bits_to_f32(x[r * k + c0 + j]) : 0.0f;
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; j++) amax = fmaxf(amax, fabsf(v[j]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const float d = __fdiv_rn(amax, 127.0f);
+        int q[8];
+        int sum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            int t = 0;
+            if (amax != 0.0f) {
+                t = (int)roundf(__fdiv_rn(v[j], d));
+                t = max(-127, min(127, t));
+            }
+            q[j] = t;
+            sum += t;
+        }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            lo |= (uint32_t)(q[j] & 0xFF) << (8 * j);
+            hi |= (uint32_t)(q[4 + j] & 0xFF) << (8 * j);
+        }
+        *reinterpret_cast<uint2*>(codes + r * kp + c0) = make_uint2(lo, hi);
+        if ((threadIdx.x & 3) == 0) ds[r * (kp / 32) + c0 / 32] = make_float2(d, __fmul_rn(d, (float)sum));
+    }
+}
+
+// =====================================================================================
+// SiLU(gate) * up -> BF16.  SiLU(z) = z * sigmoid(z), sigmoid from e = exp(-|z|) so that
+// neither branch overflows.
+// Source: dense_ffn_decode_batch.rs, `forward_km_q2` (`silu_mul`).
+// =====================================================================================
+__device__ __forceinline__ float silu_mul1(float g, float u) {
+    const float e = expf(-fabsf(g));
+    const float sig = (g >= 0.0f) ? 1.0f / (1.0f + e) : e / (1.0f + e);
+    return g * sig * u;
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(256) silu_mul_kernel(const uint16_t* __restrict__ gate, const uint16_t* __restrict__ up,
+                                                       uint16_t* out, int64_t count) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    if (VEC) {
+        for (int64_t id = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; id < count / 8; id += stride) {
+            const uint4 g = *reinterpret_cast<const uint4*>(gate + 8 * id);
+            const uint4 u = *reinterpret_cast<const uint4*>(up + 8 * id);
+            const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const float a = silu_mul1(__uint_as_float(gw[j] << 16), __uint_as_float(uw[j] << 16));
+                const float b = silu_mul1(__uint_as_float(gw[j] & 0xFFFF0000u), __uint_as_float(uw[j] & 0xFFFF0000u));
+                o[j] = bf162_bits(__floats2bfloat162_rn(a, b));
+            }
+            *reinterpret_cast<uint4*>(out + 8 * id) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    } else {
+        for (int64_t id = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; id < count; id += stride) {
+            const float h = silu_mul1(bf16_bits_to_f32(gate[id]), bf16_bits_to_f32(up[id]));
+            const __nv_bfloat16 b = __float2bfloat16_rn(h);
+            out[id] = *reinterpret_cast<const uint16_t*>(&b);
+        }
+    }
+}
+
+// =====================================================================================
+// BF16 -> block_q4_K, one thread per 256-value block (the page's launch: block 128).
+// Min/max quantiser; every decision is one IEEE fp32 operation (explicit _rn intrinsics)
+// and fp16 conversions round to nearest even.
+// Source: q4k_mmq.rs, `quantize_weight_q4k`.
+// =====================================================================================
+__global__ void __launch_bounds__(128) q4k_quant_kernel(const uint16_t* __restrict__ w, uint8_t* __restrict__ out,
+                                                        int64_t n, int64_t k) {
+    const int64_t nsb = k / 256;
+    const int64_t total = n * nsb;
+    const int64_t id = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (id >= total) return;
+    const int64_t r = id / nsb, sb = id % nsb;
+    const uint16_t* src = w + r * k + sb * 256;
+    uint8_t* blk = out + id * 144;
+
+    float scale[8], negmin[8], max_scale = 0.0f, max_min = 0.0f;
+    for (int j = 0; j < 8; j++) {
+        float lo = bf16_bits_to_f32(src[32 * j]), hi = lo;
+        for (int l = 1; l < 32; l++) {
+            const float v = bf16_bits_to_f32(src[32 * j + l]);
+            if (v < lo) lo = v;
+            if (v > hi) hi = v;
+        }
+        if (lo > 0.0f) lo = 0.0f;
+        scale[j] = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+        negmin[j] = -lo;
+        if (scale[j] > max_scale) max_scale = scale[j];
+        if (negmin[j] > max_min) max_min = negmin[j];
+    }
+    const __half dh = __float2half_rn(__fdiv_rn(max_scale, 63.0f));
+    const __half mh = __float2half_rn(__fdiv_rn(max_min, 63.0f));
+    const float d = __half2float(dh), dmin = __half2float(mh);
+    int sc[8], mn[8];
+    for (int j = 0; j < 8; j++) {
+        sc[j] = d > 0.0f ? max(0, min(63, (int)roundf(__fdiv_rn(scale[j], d)))) : 0;
+        mn[j] = dmin > 0.0f ? max(0, min(63, (int)roundf(__fdiv_rn(negmin[j], dmin)))) : 0;
+    }
+    const uint16_t dbits = *reinterpret_cast<const uint16_t*>(&dh), mbits = *reinterpret_cast<const uint16_t*>(&mh);
+    uint32_t head = (uint32_t)dbits | ((uint32_t)mbits << 16);
+    uint8_t s12[12];
+    for (int j = 0; j < 4; j++) {
+        s12[j] = (uint8_t)((sc[j] & 63) | ((sc[j + 4] >> 4) << 6));
+        s12[j + 4] = (uint8_t)((mn[j] & 63) | ((mn[j + 4] >> 4) << 6));
+    }
+    for (int j = 4; j < 8; j++) s12[j + 4] = (uint8_t)((sc[j] & 15) | ((mn[j] & 15) << 4));
+    // 144-byte blocks are 16-byte aligned (144 = 9 * 16) when the output base is.
+    uint32_t words[36];
+    words[0] = head;
+    for (int i = 0; i < 3; i++)
+        words[1 + i] = (uint32_t)s12[4 * i] | ((uint32_t)s12[4 * i + 1] << 8) | ((uint32_t)s12[4 * i + 2] << 16) |
+                       ((uint32_t)s12[4 * i + 3] << 24);
+    for (int c = 0; c < 4; c++) {
+        const int j0 = 2 * c, j1 = 2 * c + 1;
+        const float ds0 = __fmul_rn(d, (float)sc[j0]), dm0 = __fmul_rn(dmin, (float)mn[j0]);
+        const float ds1 = __fmul_rn(d, (float)sc[j1]), dm1 = __fmul_rn(dmin, (float)mn[j1]);
+        for (int l4 = 0; l4 < 8; l4++) {
+            uint32_t word = 0;
+            for (int b = 0; b < 4; b++) {
+                const int l = 4 * l4 + b;
+                int q0 = 0, q1 = 0;
+                if (ds0 > 0.0f)
+                    q0 = max(0, min(15, (int)roundf(__fdiv_rn(__fadd_rn(bf16_bits_to_f32(src[32 * j0 + l]), dm0), ds0))));
+                if (ds1 > 0.0f)
+                    q1 = max(0, min(15, (int)roundf(__fdiv_rn(__fadd_rn(bf16_bits_to_f32(src[32 * j1 + l]), dm1), ds1))));
+                word |= (uint32_t)(q0 | (q1 << 4)) << (8 * b);
+            }
+            words[4 + 8 * c + l4] = word;
+        }
+    }
+    uint4* dst = reinterpret_cast<uint4*>(blk);
+    for (int i = 0; i < 9; i++) dst[i] = make_uint4(words[4 * i], words[4 * i + 1], words[4 * i + 2], words[4 * i + 3]);
+}
+
+static int grid_for(int64_t work_items, int threads) {
+    const int64_t want = (work_items + threads - 1) / threads;
+    const int64_t cap = (int64_t)sm_count() * 16;  // grid-stride beyond 16 CTAs per SM
+    return (int)(want < 1 ? 1 : (want > cap ? cap : want));
+}
+
+}  // namespace bq8
+
+using namespace bq8;
+
+extern "C" {
+
+int bq_q2_pack(const uint8_t* codes, const uint16_t* scales, void* out, uint32_t n, uint32_t k, uint32_t group,
+               bq_stream_t stream) {
+    if (group == 0 || group % 128 != 0 || k % 128 != 0 || k % group != 0)
+        return fail(BQ_ERR_INVALID, "bq_q2_pack: need k %% 128 == 0, group %% 128 == 0, k %% group == 0 (k=%u group=%u)",
+                    k, group);
+    if (n == 0 || k == 0) return ok();
+    if (!codes || !scales || !out) return fail(BQ_ERR_INVALID, "bq_q2_pack: NULL pointer");
+    if (!aligned16(codes) || !aligned16(scales) || !aligned16(out))
+        return fail(BQ_ERR_INVALID, "bq_q2_pack: pointers must be 16-byte aligned");
+    const int64_t nsc = (int64_t)n * (k / group);
+    const int64_t work = (int64_t)n * (k / 16) > nsc ? (int64_t)n * (k / 16) : nsc;
+    q2_pack_kernel<<<grid_for(work, 256), 256, 0, (cudaStream_t)stream>>>(codes, scales, (uint8_t*)out, n, k, nsc);
+    return check_launch("bq_q2_pack");
+}
+
+int dequant_q2_to_bf16(const bq_q2_weight* w, uint16_t* out, bq_stream_t stream) {
+    int st = check_q2(w, "dequant_q2_to_bf16");
+    if (st) return st;
+    if (w->n == 0 || w->k == 0) return ok();
+    if (!out || !aligned16(out)) return fail(BQ_ERR_INVALID, "dequant_q2_to_bf16: out NULL or not 16-byte aligned");
+    const int64_t work = (int64_t)w->n * (w->k / 32);
+    q2_dequant_kernel<<<grid_for(work, 256), 256, 0, (cudaStream_t)stream>>>((const uint8_t*)w->data, out, w->n, w->k,
+                                                                            (int)w->group);
+    return check_launch("dequant_q2_to_bf16");
+}
+
+int quantize_act_q8_1(const uint16_t* x, void* act_q8, uint32_t m, uint32_t k, bq_stream_t stream) {
+    if (m == 0 || k == 0) return ok();
+    if (!x || !act_q8) return fail(BQ_ERR_INVALID, "quantize_act_q8_1: NULL pointer");
+    if (!aligned16(x) || !aligned16(act_q8))
+        return fail(BQ_ERR_INVALID, "quantize_act_q8_1: pointers must be 16-byte aligned");
+    const int64_t kp = ((int64_t)k + 255) / 256 * 256;
+    int8_t* codes = (int8_t*)act_q8;
+    float2* ds = (float2*)((uint8_t*)act_q8 + (int64_t)m * kp);
+    const int64_t work = (int64_t)m * kp / 8;
+    if (k % 8 == 0)
+        q8_1_kernel<true><<<grid_for(work, 256), 256, 0, (cudaStream_t)stream>>>(x, codes, ds, m, k, kp);
+    else
+        q8_1_kernel<false><<<grid_for(work, 256), 256, 0, (cudaStream_t)stream>>>(x, codes, ds, m, k, kp);
+    return check_launch("quantize_act_q8_1");
+}
+
+int silu_mul_bf16(const uint16_t* gate, const uint16_t* up, uint16_t* out, size_t count, bq_stream_t stream) {
+    if (count == 0) return ok();
+    if (!gate || !up || !out) return fail(BQ_ERR_INVALID, "silu_mul_bf16: NULL pointer");
+    const bool vec = aligned16(gate) && aligned16(up) && aligned16(out) && count % 8 == 0;
+    if (vec)
+        silu_mul_kernel<true><<<grid_for((int64_t)count / 8, 256), 256, 0, (cudaStream_t)stream>>>(gate, up, out, count);
+    else
+        silu_mul_kernel<false><<<grid_for((int64_t)count, 256), 256, 0, (cudaStream_t)stream>>>(gate, up, out, count);
+    return check_launch("silu_mul_bf16");
+}
+
+int quantize_weight_q4k(const uint16_t* w, void* out_q4k, uint32_t n, uint32_t k, bq_stream_t stream) {
+    if (k % 256 != 0) return fail(BQ_ERR_INVALID, "quantize_weight_q4k: k %u must be a multiple of 256", k);
+    if (n == 0 || k == 0) return ok();
+    if (!w || !out_q4k || !aligned16(w) || !aligned16(out_q4k))
+        return fail(BQ_ERR_INVALID, "quantize_weight_q4k: pointers must be non-NULL and 16-byte aligned");
+    const int64_t total = (int64_t)n * (k / 256);
+    const int64_t blocks = (total + 127) / 128;
+    if (blocks > 0x7fffffff) return fail(BQ_ERR_INVALID, "quantize_weight_q4k: weight too large");
+    q4k_quant_kernel<<<(unsigned)blocks, 128, 0, (cudaStream_t)stream>>>(w, (uint8_t*)out_q4k, n, k);
+    return check_launch("quantize_weight_q4k");
+}
+
+}  // extern "C"
