@@ -272,7 +272,8 @@ def run_ours(args, rank, local, world):
 
     # kernel-only per-launch durations (event-bracketed single launches, not graphed)
     def one(i, m):
-        (B.q2_gemv if m == 1 else B.q2_gemv_batchm)(x1 if m == 1 else x4, layers[i % L], out=(y1 if m == 1 else y4)[i % L])
+        (B.q2_gemv if m == 1 else B.q2_gemv_batchm)(x1 if m == 1 else x4, layers[i % L],
+                                                    out=(y1 if m == 1 else y4)[i % L])
     kern = {}
     for m in (1, 4):
         ts = []
@@ -373,7 +374,8 @@ def measure_rows(args, dev, hbm_peak, bf16_peak):
         gs = torch.empty((m, inter), dtype=torch.bfloat16, device=dev)
         us = torch.empty((m, inter), dtype=torch.bfloat16, device=dev)
         out = torch.empty((m, hidden), dtype=torch.bfloat16, device=dev)
-        g = _graph(lambda: [B.ffn_q2_km(xm, *s, gate_scratch=gs, up_scratch=us, out=out) for s in sets])
+        g = _graph(lambda: [B.ffn_q2_km(xm, *s, gate_scratch=gs, up_scratch=us, out=out)
+                            for s in sets])
         t = _time_graph(g, reps) / len(sets)
         rows["a4_ffn_q2_m%d" % m] = {"us": t * 1e6, "weight_GBps": chain_bytes / t / 1e9,
                                      "frac_hbm": chain_bytes / t / 1e9 / hbm_peak, "launches": 4}

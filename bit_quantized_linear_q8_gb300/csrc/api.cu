@@ -73,13 +73,19 @@ static PFN_encodeTiled encode_fn() {
 
 int make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint64_t stride_bytes,
                     uint32_t box_bytes, uint32_t box_rows, bool swizzle128, const char* who) {
+    return make_tmap_2d(map, base, 1, row_bytes, rows, stride_bytes, box_bytes, box_rows, swizzle128, who);
+}
+
+int make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t row_elems, uint64_t rows,
+                 uint64_t stride_bytes, uint32_t box_elems, uint32_t box_rows, bool swizzle128, const char* who) {
     PFN_encodeTiled fn = encode_fn();
     if (!fn) return fail(BQ_ERR_UNSUPPORTED, "%s: cuTensorMapEncodeTiled unavailable from the driver", who);
-    const cuuint64_t dims[2] = {row_bytes, rows};
+    const cuuint64_t dims[2] = {row_elems, rows};
     const cuuint64_t strides[1] = {stride_bytes};
-    const cuuint32_t box[2] = {box_bytes, box_rows};
+    const cuuint32_t box[2] = {box_elems, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+    const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(BQ_ERR_INVALID, "%s: tensor map encoding failed (CUresult %d)", who, (int)r);

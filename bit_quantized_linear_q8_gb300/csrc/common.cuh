@@ -32,6 +32,10 @@ int check_q2(const bq_q2_weight* w, const char* who);
 int make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
                     uint64_t stride_bytes, uint32_t box_bytes, uint32_t box_rows, bool swizzle128,
                     const char* who);
+// Same for 1- or 2-byte elements: matrix [rows][row_elems], box [box_rows][box_elems]
+// (box_elems <= 256).
+int make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t row_elems, uint64_t rows,
+                 uint64_t stride_bytes, uint32_t box_elems, uint32_t box_rows, bool swizzle128, const char* who);
 
 // Reads and clears each translation unit's device status word (nonzero after a bounded
 // wait gave up).
@@ -80,9 +84,8 @@ __device__ __forceinline__ void mma_s8u8_16832(int (&d)[4], uint32_t a0, uint32_
 }
 
 // ------------------------------------------------------------------ mbarrier / TMA
-// Every wait is bounded: after ~1 s of spinning the caller gets `false`, records the
-// failure in its status word and winds down instead of hanging the GPU.
-constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;
+// Every wait is bounded: after over a second of polling the caller gets `false`, records
+// the failure in its status word and winds down instead of hanging the GPU.
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -107,12 +110,15 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("{\n.reg .b64 st;\nmbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(smem_u32(bar)) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// Non-blocking probe of phase `parity` of `bar`.  (mbarrier.try_wait may park the warp for
+// microseconds before it returns false, which the short stages of these kernels cannot
+// afford, so waits poll test_wait with a short sleep instead.)
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
         "{\n"
         ".reg .pred p;\n"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
         "selp.u32 %0, 1, 0, p;\n"
         "}\n"
         : "=r"(done)
@@ -121,14 +127,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return done != 0;
 }
 
-// Waits for phase `parity` of `bar` to complete; false after WAIT_LIMIT_CYCLES.
+// Waits for phase `parity` of `bar` to complete.  Polls with a short sleep; gives up (false)
+// after ~2^26 polls (well over a second), so a wait that can never complete ends the kernel
+// instead of hanging the GPU.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long start = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - start > WAIT_LIMIT_CYCLES) return false;
+    if (mbar_test(bar, parity)) return true;
+    for (uint32_t it = 0; it < (1u << 26); it++) {
+        __nanosleep(32);
+        if (mbar_test(bar, parity)) return true;
     }
-    return true;
+    return false;
+}
+
+// (a & b) | c in one LOP3 with all three operands in registers.
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
 }
 
 // 2-D TMA tile load global -> shared, completion counted on `bar` (bytes).
@@ -139,9 +154,56 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// Cooperative copy of `bytes` contiguous bytes global -> shared (both 16-byte aligned,
+// bytes % 2 == 0): 16-byte vectors, every load of a thread issued before its stores so a
+// thread pays one memory latency, not one per element.
+__device__ __forceinline__ void copy_to_smem(void* dst, const void* src, int bytes, int tid, int nthreads) {
+    const int nvec = bytes >> 4;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    constexpr int B = 8;
+    for (int base = tid; base < nvec; base += B * nthreads) {
+        uint4 v[B];
+#pragma unroll
+        for (int j = 0; j < B; j++) {
+            const int i = base + j * nthreads;
+            if (i < nvec) v[j] = __ldg(s4 + i);
+        }
+#pragma unroll
+        for (int j = 0; j < B; j++) {
+            const int i = base + j * nthreads;
+            if (i < nvec) d4[i] = v[j];
+        }
+    }
+    const uint16_t* s2 = reinterpret_cast<const uint16_t*>(src);
+    uint16_t* d2 = reinterpret_cast<uint16_t*>(dst);
+    for (int i = (nvec << 3) + tid; i < (bytes >> 1); i += nthreads) d2[i] = s2[i];
+}
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
+
+// D = A(16x32 e4m3, row) * B(32x8 e4m3, col) + C, fp32 accumulate (legacy warp MMA).
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 1-D bulk copy global -> shared (16-byte aligned, size % 16 == 0), completion on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Programmatic dependent launch: let the next grid start / wait for the previous grid.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t bf162_bits(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
 __device__ __forceinline__ __nv_bfloat162 bits_bf162(uint32_t u) { return *reinterpret_cast<__nv_bfloat162*>(&u); }

@@ -3,28 +3,30 @@
 // Source: init_q2.rs `set_packed_q2_qkvz` (decode runs `q2_0_gemv_vec`) and
 // dense_ffn_decode_batch.rs `forward_km_q2` (`q2_0_gemv_vec_batchm` for gate/up/down).
 //
-// Design (GB300).  The packed weight (2.125 bits per weight) is the only large stream, so
-// the kernel is built to keep HBM busy:
+// Design (GB300).  The packed weight (2.125 bits per weight) is the only large stream; the
+// kernel must keep the per-weight instruction count low and stay within the native legacy
+// tensor pipe.  On sm_103a the warp-level BF16 MMA (m16n8k16, HMMA) is native; the e4m3 and
+// int8 forms are not (they expand into conversions plus HMMAs), so:
 //
-//  * Staging: one producer warp streams the CTA's rows through a 4-stage shared-memory
-//    ring with TMA (cp.async.bulk.tensor, 16 rows x 128 bytes per box, 128-byte swizzle,
-//    mbarrier completion).  A stage is a 256-byte chunk of every row of the CTA (8 pack
-//    blocks of 128 codes); up to four chunks are in flight per SM without costing
-//    registers.  Every wait is bounded.
-//  * Compute: eight consumer warps; warp w takes pack block w of each chunk for all of
-//    the CTA's row tiles (16 rows each).  The multiply-accumulates for all m <= 8 rows go
-//    to the tensor cores through the warp-level MMA m16n8k16 (A = 16 weight rows x 16
-//    columns, B = 16 columns x 8 activation rows), so the CUDA cores only unpack:
-//      - one AND/OR (lop3) per pair of codes drops a 2-bit code into the mantissa of BF16
-//        1.0 in each 16-bit half, v = 1 + c*s with s = 2^-7, 2^-5 or 2^-3 depending on
-//        the code's bit position (three of the four positions need no shift);
-//      - the activation fragment is built once per pack block per warp, each column
-//        pre-multiplied by 1/s (exact, a power of two) and permuted to the lanes' code
-//        order, so sum(v*x/s) = sum(x/s) + sum(c*x);
-//      - sum((c-2)*x) = sum(v*x/s) - sum((1/s + 2)*x); the correction comes from eight
-//        extra MMAs per pack block with a constant A of -(1 + 2s) and seeds every tile's
-//        accumulator, so it costs nothing per row tile;
-//      - each 128-column group is scaled by its BF16 scale d (held in shared memory).
+//  * Weights (A operand, 16 rows x 16 columns per MMA): one lop3 per pair of codes drops a
+//    2-bit code into the mantissa of BF16 1.0 in each 16-bit half, v = 1 + c*s with
+//    s = 2^-7, 2^-5 or 2^-3 depending on the code's bit position (three of the four
+//    positions need no shift).
+//  * Activations (B operand, 16 columns x 8 rows): per pack block each warp builds its
+//    fragment from the staged activations, each column pre-multiplied by 1/s (exact: a
+//    power of two) and permuted to the lanes' code order, so sum(v*x/s) = sum(x/s) +
+//    sum(c*x).
+//  * sum((c - 2) x) = sum(v x/s) - sum((1/s + 2) x): the second sum, per activation row and
+//    128-column block, is formed on the CUDA cores and seeds every tile's accumulator; each
+//    128-column group is then scaled by its BF16 d.
+//  * Staging: the CTA's rows stream through a shared-memory ring of up to four stages: per
+//    chunk two TMA boxes of all the CTA's rows x 128 bytes (128-byte swizzle) for the codes
+//    and 256-column boxes for the activations, mbarrier completion.  There is no producer
+//    warp: the last warp to release a stage requests the next chunk into it.  Every wait
+//    is bounded.
+//  * Compute: eight warps; warp w takes pack block w of each 256-byte chunk for all of the
+//    CTA's 16-row tiles.  MMAs are issued column-step outer, tile inner, so consecutive MMAs
+//    are independent.
 //  * Work split: CTA c takes a contiguous range of <= T row tiles (grid = SM count when
 //    possible, so every SM streams the same number of rows); the warps' partial sums are
 //    reduced through shared memory and stored as BF16.
@@ -32,12 +34,14 @@
 
 namespace bq8 {
 
-constexpr int GEMV_CWARPS = 8;                        // consumer warps = pack blocks per chunk
-constexpr int GEMV_THREADS = (GEMV_CWARPS + 1) * 32;  // + one producer warp
+constexpr int GEMV_PBLK = 8;                          // pack blocks per chunk (256 bytes of a row)
+constexpr int GEMV_CWARPS = 8;                        // warps: one per pack block
+constexpr int GEMV_THREADS = GEMV_CWARPS * 32;
 constexpr int GEMV_MAX_T = 8;                         // row tiles per CTA (128 rows)
-constexpr int GEMV_STAGES = 4;
-constexpr int GEMV_BOX = 16 * 128;                    // one TMA box: 16 rows x 128 bytes
-constexpr int GEMV_MAX_SCALE_BYTES = 64 * 1024;
+constexpr int GEMV_MAX_STAGES = 4;
+constexpr int GEMV_BOX = 16 * 128;                    // one codes box: 16 rows x 128 bytes
+constexpr int GEMV_XBOX = 256;                        // activations per x box row (bf16)
+constexpr int GEMV_SMEM_LIMIT = 225 * 1024;
 
 static __device__ unsigned int g_gemv_status;
 
@@ -49,71 +53,99 @@ unsigned int gemv_status_take() {
     return v;
 }
 
-// Code pair `SUB` (0..7) of a packed 32-bit word: bytes (0,2) for SUB < 4, bytes (1,3)
-// otherwise; sub-block i = SUB & 3 sits in bits 2i of each byte.
+// Code pair SUB (0..7) of a packed 32-bit word: bytes (0,2) for SUB < 4, bytes (1,3)
+// otherwise; sub-block i = SUB & 3 sits in bits 2i of each byte.  mask[i] holds the code
+// mask of position i; `one` is bf16x2 (1.0, 1.0).
 template <int SUB>
-__device__ __forceinline__ uint32_t unpack_pair(uint32_t w) {
-    constexpr uint32_t ONE = 0x3F803F80u;  // bf16x2 (1.0, 1.0)
-    if constexpr (SUB == 0) return (w & 0x00030003u) | ONE;
-    if constexpr (SUB == 1) return (w & 0x000C000Cu) | ONE;
-    if constexpr (SUB == 2) return (w & 0x00300030u) | ONE;
-    if constexpr (SUB == 3) return ((w >> 2) & 0x00300030u) | ONE;
-    if constexpr (SUB == 4) return ((w >> 8) & 0x00030003u) | ONE;
-    if constexpr (SUB == 5) return ((w >> 8) & 0x000C000Cu) | ONE;
-    if constexpr (SUB == 6) return ((w >> 8) & 0x00300030u) | ONE;
-    return ((w >> 10) & 0x00300030u) | ONE;
+__device__ __forceinline__ uint32_t unpack_pair(uint32_t w, const uint32_t (&mask)[3], uint32_t one) {
+    if constexpr (SUB < 3) return and_or(w, mask[SUB], one);
+    if constexpr (SUB == 3) return and_or(w >> 2, mask[2], one);
+    if constexpr (SUB < 7) return and_or(w >> 8, mask[SUB - 4], one);
+    return and_or(w >> 10, mask[2], one);
 }
 
 template <int RHO>
-__device__ __forceinline__ uint32_t unpack_rho(uint2 w) {
-    return unpack_pair<RHO & 7>((RHO >> 3) ? w.y : w.x);
+__device__ __forceinline__ uint32_t unpack_rho(uint2 w, const uint32_t (&mask)[3], uint32_t one) {
+    return unpack_pair<RHO & 7>((RHO >> 3) ? w.y : w.x, mask, one);
 }
 
-// -(1 + 2s) for sub-block i (s = 2^-7, 2^-5, 2^-3, 2^-3), as bf16x2.
-__device__ __forceinline__ uint32_t neg_offset_coef(int i) {
-    return i == 0 ? 0xBF82BF82u : (i == 1 ? 0xBF88BF88u : 0xBFA0BFA0u);
+// Column step MU (16 columns) of every tile of the warp: tile-inner, so the TQ MMAs in a
+// row are independent.
+template <int MU, int TQ>
+__device__ __forceinline__ void gemv_step(float (&acc)[TQ][4], const uint2 (&wa)[TQ], const uint2 (&wb)[TQ],
+                                          const uint32_t (&b)[16], const uint32_t (&mask)[3], uint32_t one) {
+#pragma unroll
+    for (int q = 0; q < TQ; q++)
+        mma_bf16_16816(acc[q], unpack_rho<2 * MU>(wa[q], mask, one), unpack_rho<2 * MU>(wb[q], mask, one),
+                       unpack_rho<2 * MU + 1>(wa[q], mask, one), unpack_rho<2 * MU + 1>(wb[q], mask, one),
+                       b[2 * MU], b[2 * MU + 1], acc[q]);
 }
 
-// B-fragment registers of lane (g, t) for one pack block: activation row g, columns
-// 32i + 8t + {0..7} of the block, paired as the codes are and scaled by 1/s.
-__device__ __forceinline__ void build_bfrag(uint32_t (&b)[16], const uint4 (&X)[4]) {
+// B fragment of lane (g, t) for one pack block, from activation row g's 128 columns (X[i]
+// = columns 32i + 8t .. 32i + 8t + 7): register rho = 8w + sub pairs columns 4w + bo and
+// 4w + bo + 2 of run i = sub & 3 (bo = sub >> 2), scaled by 1/s_i = 128, 32, 8, 8.  Also
+// returns this lane's share of -sum((1/s + 2) x).
+__device__ __forceinline__ float build_bfrag(uint32_t (&b)[16], const uint4 (&X)[4]) {
     const __nv_bfloat162 scl[4] = {__floats2bfloat162_rn(128.f, 128.f), __floats2bfloat162_rn(32.f, 32.f),
                                    __floats2bfloat162_rn(8.f, 8.f), __floats2bfloat162_rn(8.f, 8.f)};
+    float off = 0.f;
 #pragma unroll
-    for (int rho = 0; rho < 16; rho++) {
-        const int w = rho >> 3, sub = rho & 7, i = sub & 3, hi = sub >> 2;
-        const uint32_t a = w ? X[i].z : X[i].x;
-        const uint32_t c = w ? X[i].w : X[i].y;
-        const uint32_t pr = __byte_perm(a, c, hi ? 0x7632 : 0x5410);
-        b[rho] = bf162_bits(__hmul2(bits_bf162(pr), scl[i]));
+    for (int i = 0; i < 4; i++) {
+        const float coef = i == 0 ? -130.f : (i == 1 ? -34.f : -10.f);
+        const uint32_t wds[4] = {X[i].x, X[i].y, X[i].z, X[i].w};
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; j++) s += __uint_as_float(wds[j] << 16) + __uint_as_float(wds[j] & 0xFFFF0000u);
+        off = fmaf(coef, s, off);
+#pragma unroll
+        for (int w = 0; w < 2; w++) {
+#pragma unroll
+            for (int bo = 0; bo < 2; bo++) {
+                const uint32_t pr = __byte_perm(w ? X[i].z : X[i].x, w ? X[i].w : X[i].y, bo ? 0x7632 : 0x5410);
+                b[8 * w + 4 * bo + i] = bf162_bits(__hmul2(bits_bf162(pr), scl[i]));
+            }
+        }
     }
+    return off;
 }
 
-__device__ __forceinline__ void load_x(uint4 (&X)[4], const uint16_t* __restrict__ x, int k, int p, int g, int t,
-                                       bool valid) {
-    if (valid) {
-        const uint16_t* xr = x + (size_t)g * k + (p << 7) + (t << 3);
-#pragma unroll
-        for (int i = 0; i < 4; i++) X[i] = ldg_nc128(xr + 32 * i);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 4; i++) X[i] = make_uint4(0, 0, 0, 0);
-    }
+// Shared-memory layout of one stage: codes boxes [2 halves][T*16 rows][128 B] (128-byte
+// swizzle), then the activation boxes [4][m rows][256 bf16].
+template <int T>
+struct GemvStage {
+    static constexpr int CODES = 2 * T * GEMV_BOX;
+    __host__ __device__ static int bytes(int m) { return CODES + 4 * m * GEMV_XBOX * 2; }
+};
+
+// Requests chunk c into stage s: the codes of the CTA's rows (one box per 128-byte half;
+// `tmap` has a box of exactly nt*16 rows) and the chunk's activation columns.
+template <int T>
+__device__ __forceinline__ void gemv_issue(uint8_t* stages, int stage_bytes, uint64_t* full, const CUtensorMap* tmap,
+                                           const CUtensorMap* xmap, int c, int s, int nt, int r0, int m) {
+    uint8_t* dst = stages + s * stage_bytes;
+    mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * nt * GEMV_BOX + 4 * m * GEMV_XBOX * 2));
+    tma_load_2d(dst, tmap, c * 256, r0, &full[s]);
+    tma_load_2d(dst + T * GEMV_BOX, tmap, c * 256 + 128, r0, &full[s]);
+    for (int j = 0; j < 4; j++)
+        tma_load_2d(dst + GemvStage<T>::CODES + j * m * GEMV_XBOX * 2, xmap, c * (GEMV_PBLK * 128) + j * GEMV_XBOX, 0,
+                    &full[s]);
 }
 
 template <int T>
 __global__ void __launch_bounds__(GEMV_THREADS, 1)
-    q2_gemv_kernel(const __grid_constant__ CUtensorMap tmap, const uint16_t* __restrict__ x,
-                   const uint16_t* __restrict__ scales, uint16_t* __restrict__ y, int m, int n, int k, int group,
-                   int ntiles) {
-    constexpr int STAGE_BYTES = 2 * T * GEMV_BOX;
+    q2_gemv_kernel(const __grid_constant__ CUtensorMap tmap_full, const __grid_constant__ CUtensorMap tmap_less,
+                   const __grid_constant__ CUtensorMap xmap, const uint16_t* __restrict__ scales,
+                   uint16_t* __restrict__ y, int m, int n, int k, int group, int ntiles, int nstages) {
+    constexpr int TQ = T;  // tiles per warp
     extern __shared__ uint8_t smem_raw[];
     uint8_t* stages = align1024(smem_raw);
+    const int stage_bytes = (GemvStage<T>::bytes(m) + 1023) & ~1023;
     const int G = k / group;
-    uint16_t* sc_s = reinterpret_cast<uint16_t*>(stages + GEMV_STAGES * STAGE_BYTES);
-    uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(sc_s + 16 * T * G) + 7) & ~uintptr_t(7));
-    uint64_t* full = bars;
-    uint64_t* empty = bars + GEMV_STAGES;
+    // group scales as fp32 pairs (row r, row r + 8) per (tile, group, g)
+    float2* sc_s = reinterpret_cast<float2*>(stages + nstages * stage_bytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sc_s + 8 * T * G);
+    uint32_t* released = reinterpret_cast<uint32_t*>(full + GEMV_MAX_STAGES);  // per stage: warps done with it
+    int* issued = reinterpret_cast<int*>(released + GEMV_MAX_STAGES);          // per stage: last chunk requested
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
@@ -121,112 +153,144 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1)
     const int nt = (int)((int64_t)(blockIdx.x + 1) * ntiles / gridDim.x) - tile0;
     const int r0 = tile0 * 16;
     const int P = k >> 7;
-    const int nch = (P + GEMV_CWARPS - 1) / GEMV_CWARPS;
+    const int nch = (P + GEMV_PBLK - 1) / GEMV_PBLK;
+    const int pre = nch < nstages ? nch : nstages;
+    const CUtensorMap* tmap = nt == T ? &tmap_full : &tmap_less;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < GEMV_STAGES; s++) {
+        for (int s = 0; s < nstages; s++) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], GEMV_CWARPS);
+            released[s] = 0;
+            issued[s] = s < pre ? s : -1;
         }
         fence_barrier_init();
+        for (int c = 0; c < pre; c++) gemv_issue<T>(stages, stage_bytes, full, tmap, &xmap, c, c, nt, r0, m);
     }
-    for (int idx = threadIdx.x; idx < nt * 16 * G; idx += blockDim.x) {
-        const int row = r0 + idx / G;
-        sc_s[idx] = row < n ? scales[(size_t)row * G + idx % G] : (uint16_t)0;
+    // this CTA's group scales, as (row 16tau + g, row 16tau + g + 8) fp32 pairs: element
+    // e = (8tau + gg)*G + gi runs along a row, so the loads coalesce; eight per thread in flight
+    for (int base = 0; base < 8 * T * G; base += 8 * GEMV_THREADS) {
+        uint16_t va[8], vb[8];
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+            const int e = base + u * GEMV_THREADS + threadIdx.x;
+            const int gi = e % G, pr = e / G, tau = pr >> 3;
+            const int ra = r0 + tau * 16 + (pr & 7), rb = ra + 8;
+            va[u] = e < 8 * T * G && tau < nt && ra < n ? __ldg(scales + (size_t)ra * G + gi) : (uint16_t)0;
+            vb[u] = e < 8 * T * G && tau < nt && rb < n ? __ldg(scales + (size_t)rb * G + gi) : (uint16_t)0;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+            const int e = base + u * GEMV_THREADS + threadIdx.x;
+            const int gi = e % G, pr = e / G;
+            if (e < 8 * T * G)
+                sc_s[((pr >> 3) * G + gi) * 8 + (pr & 7)] = make_float2(bf16_bits_to_f32(va[u]), bf16_bits_to_f32(vb[u]));
+        }
     }
     __syncthreads();
 
     bool failed = false;
-    float tot[T][4];
+    float tot[TQ][4];
 #pragma unroll
-    for (int tau = 0; tau < T; tau++) tot[tau][0] = tot[tau][1] = tot[tau][2] = tot[tau][3] = 0.f;
-
-    if (warp == GEMV_CWARPS) {
-        // ---------------------------------------------------------------- producer
-        if (lane == 0) {
-            for (int c = 0; c < nch; c++) {
-                const int s = c % GEMV_STAGES;
-                if (c >= GEMV_STAGES && !mbar_wait(&empty[s], ((c / GEMV_STAGES) - 1) & 1)) {
-                    failed = true;
-                    break;
-                }
-                mbar_arrive_expect_tx(&full[s], 2 * nt * GEMV_BOX);
-                uint8_t* dst = stages + s * STAGE_BYTES;
-                for (int h = 0; h < 2; h++)
-                    for (int tau = 0; tau < nt; tau++)
-                        tma_load_2d(dst + (h * T + tau) * GEMV_BOX, &tmap, c * 256 + h * 128, r0 + 16 * tau, &full[s]);
-            }
-            // wind down: every issued chunk must have landed before the CTA may exit
-            const int first = nch > GEMV_STAGES ? nch - GEMV_STAGES : 0;
-            for (int c = first; c < nch && !failed; c++)
-                if (!mbar_wait(&full[c % GEMV_STAGES], (c / GEMV_STAGES) & 1)) failed = true;
+    for (int q = 0; q < TQ; q++) tot[q][0] = tot[q][1] = tot[q][2] = tot[q][3] = 0.f;
+    const int pb = warp;
+    const int hb = pb >> 2;                                  // which 128-byte half of the chunk
+    const int jch = ((pb & 3) << 1) | (t >> 1);              // 16-byte chunk holding bytes 8t..8t+7
+    const int offw = ((jch ^ g) << 4) + ((t & 1) << 3);      // swizzled: (line & 7) == g
+    const uint32_t mask[3] = {0x00030003u, 0x000C000Cu, 0x00300030u};
+    const uint32_t one = 0x3F803F80u;
+    for (int c = 0; c < nch; c++) {
+        const int s = c % nstages;
+        const int p = c * GEMV_PBLK + pb;
+        if (!mbar_wait(&full[s], (c / nstages) & 1)) {
+            failed = true;
+            break;
         }
-    } else {
-        // ---------------------------------------------------------------- consumers
-        const int pb = warp;
-        const int half = pb >> 2;
-        const int jchunk = ((pb & 3) << 1) | (t >> 1);   // 16-byte chunk within the 128-byte line
-        const int inner = (t & 1) << 3;
-        uint4 xc[4], xn[4];
-        load_x(xc, x, k, pb, g, t, g < m && pb < P);
-        for (int c = 0; c < nch; c++) {
-            const int s = c % GEMV_STAGES;
-            const int p = c * GEMV_CWARPS + pb;
-            const int pnext = p + GEMV_CWARPS;
-            load_x(xn, x, k, pnext, g, t, g < m && pnext < P && c + 1 < nch);
-            if (!mbar_wait(&full[s], (c / GEMV_STAGES) & 1)) {
-                failed = true;
-                break;
+        if (p < P) {
+            const uint8_t* st = stages + s * stage_bytes;
+            uint32_t b[16];
+            float offp = 0.f;
+            if (g < m) {
+                const uint8_t* xs = st + GemvStage<T>::CODES + ((pb >> 1) * m + g) * (GEMV_XBOX * 2) +
+                                    (((pb & 1) << 7) + (t << 3)) * 2;
+                uint4 X[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) X[i] = *reinterpret_cast<const uint4*>(xs + 64 * i);
+                offp = build_bfrag(b, X);
+            } else {
+#pragma unroll
+                for (int r = 0; r < 16; r++) b[r] = 0u;
             }
-            if (p < P) {
-                uint32_t b[16];
-                build_bfrag(b, xc);
-                float neg[4] = {0.f, 0.f, 0.f, 0.f};
+            // -sum((1/s + 2) x) of activation rows 2t and 2t+1 (lanes 8t.. and 8t+4.. hold them)
+            offp += __shfl_xor_sync(0xffffffffu, offp, 1);
+            offp += __shfl_xor_sync(0xffffffffu, offp, 2);
+            const float off0 = __shfl_sync(0xffffffffu, offp, 8 * t);
+            const float off1 = __shfl_sync(0xffffffffu, offp, 8 * t + 4);
+            uint2 wa[TQ], wb[TQ];
+            const int gi = (p << 7) / group;
 #pragma unroll
-                for (int mu = 0; mu < 8; mu++) {
-                    const uint32_t c0 = neg_offset_coef((2 * mu) & 3), c1 = neg_offset_coef((2 * mu + 1) & 3);
-                    mma_bf16_16816(neg, c0, c0, c1, c1, b[2 * mu], b[2 * mu + 1], neg);
-                }
-                const int gi = (p << 7) / group;
-                const uint8_t* st = stages + s * STAGE_BYTES;
-                const int off = ((jchunk ^ g) << 4) + inner;   // swizzled: (line & 7) == g
+            for (int q = 0; q < TQ; q++) {
+                const int tau = q;
+                const bool v = tau < nt;
+                const uint8_t* la = st + (hb * T * 16 + tau * 16 + g) * 128 + offw;
+                wa[q] = v ? *reinterpret_cast<const uint2*>(la) : make_uint2(0, 0);
+                wb[q] = v ? *reinterpret_cast<const uint2*>(la + 8 * 128) : make_uint2(0, 0);
+            }
+            float acc[TQ][4];
 #pragma unroll
-                for (int tau = 0; tau < T; tau++) {
-                    if (tau < nt) {
-                        const int line = (half * T + tau) * 16 + g;
-                        const uint2 wa = *reinterpret_cast<const uint2*>(st + line * 128 + off);
-                        const uint2 wb = *reinterpret_cast<const uint2*>(st + (line + 8) * 128 + off);
-                        const float da = bf16_bits_to_f32(sc_s[(tau * 16 + g) * G + gi]);
-                        const float db = bf16_bits_to_f32(sc_s[(tau * 16 + g + 8) * G + gi]);
-                        float acc[4] = {neg[0], neg[1], neg[2], neg[3]};
-#define BQ8_MMA(MU)                                                                                     \
-    mma_bf16_16816(acc, unpack_rho<2 * MU>(wa), unpack_rho<2 * MU>(wb), unpack_rho<2 * MU + 1>(wa),    \
-                   unpack_rho<2 * MU + 1>(wb), b[2 * MU], b[2 * MU + 1], acc);
-                        BQ8_MMA(0) BQ8_MMA(1) BQ8_MMA(2) BQ8_MMA(3) BQ8_MMA(4) BQ8_MMA(5) BQ8_MMA(6) BQ8_MMA(7)
-#undef BQ8_MMA
-                        tot[tau][0] = fmaf(da, acc[0], tot[tau][0]);
-                        tot[tau][1] = fmaf(da, acc[1], tot[tau][1]);
-                        tot[tau][2] = fmaf(db, acc[2], tot[tau][2]);
-                        tot[tau][3] = fmaf(db, acc[3], tot[tau][3]);
-                    }
+            for (int q = 0; q < TQ; q++) {
+                acc[q][0] = off0; acc[q][1] = off1; acc[q][2] = off0; acc[q][3] = off1;
+            }
+            // tiles past nt hold zero codes: their (unused) sums cost an MMA but no branch
+            gemv_step<0, TQ>(acc, wa, wb, b, mask, one);
+            gemv_step<1, TQ>(acc, wa, wb, b, mask, one);
+            gemv_step<2, TQ>(acc, wa, wb, b, mask, one);
+            gemv_step<3, TQ>(acc, wa, wb, b, mask, one);
+            gemv_step<4, TQ>(acc, wa, wb, b, mask, one);
+            gemv_step<5, TQ>(acc, wa, wb, b, mask, one);
+            gemv_step<6, TQ>(acc, wa, wb, b, mask, one);
+            gemv_step<7, TQ>(acc, wa, wb, b, mask, one);
+#pragma unroll
+            for (int q = 0; q < TQ; q++) {
+                const float2 d = sc_s[(q * G + gi) * 8 + g];
+                tot[q][0] = fmaf(d.x, acc[q][0], tot[q][0]);
+                tot[q][1] = fmaf(d.x, acc[q][1], tot[q][1]);
+                tot[q][2] = fmaf(d.y, acc[q][2], tot[q][2]);
+                tot[q][3] = fmaf(d.y, acc[q][3], tot[q][3]);
+            }
+        }
+        // release the stage; the last warp to release it requests chunk c + nstages into it
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            // counts only grow: use u of stage s is complete at 8 * (u + 1) releases
+            const uint32_t before = atomicAdd(&released[s], 1u);
+            if (before == (uint32_t)(GEMV_CWARPS * (c / nstages + 1) - 1)) {
+                const int cn = c + nstages;
+                if (cn < nch) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    issued[s] = cn;
+                    gemv_issue<T>(stages, stage_bytes, full, tmap, &xmap, cn, s, nt, r0, m);
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-#pragma unroll
-            for (int i = 0; i < 4; i++) xc[i] = xn[i];
         }
     }
     if (failed) atomicOr(&g_gemv_status, 1u);
     __syncthreads();
+    if (threadIdx.x == 0) {  // wind down: every requested chunk must have landed before the CTA exits
+        for (int s = 0; s < nstages; s++) {
+            const int c = issued[s];
+            if (c >= 0 && !mbar_wait(&full[s], (c / nstages) & 1)) atomicOr(&g_gemv_status, 1u);
+        }
+    }
+    __syncthreads();
 
     // ---------------------------------------------------------------- reduction + store
-    float* red = reinterpret_cast<float*>(stages);  // [CWARPS][T][32 lanes * 5]
-    if (warp < GEMV_CWARPS) {
+    // red[pb][tau][lane*5 + e]
+    float* red = reinterpret_cast<float*>(stages);
 #pragma unroll
-        for (int tau = 0; tau < T; tau++)
+    for (int q = 0; q < TQ; q++) {
 #pragma unroll
-            for (int e = 0; e < 4; e++) red[(warp * T + tau) * 160 + lane * 5 + e] = tot[tau][e];
+        for (int e = 0; e < 4; e++) red[(pb * T + q) * 160 + lane * 5 + e] = tot[q][e];
     }
     __syncthreads();
     const int per_col = nt * 16;
@@ -237,31 +301,39 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1)
         const int ln = (r & 7) * 4 + (j >> 1), e = (r >> 3) * 2 + (j & 1);
         float sum = 0.f;
 #pragma unroll
-        for (int w = 0; w < GEMV_CWARPS; w++) sum += red[(w * T + tau) * 160 + ln * 5 + e];
+        for (int w = 0; w < GEMV_PBLK; w++) sum += red[(w * T + tau) * 160 + ln * 5 + e];
         const __nv_bfloat16 bv = __float2bfloat16_rn(sum);
         y[(size_t)j * n + row] = *reinterpret_cast<const uint16_t*>(&bv);
     }
 }
 
 template <int T>
-static size_t gemv_smem_bytes(int G) {
-    return 1024 + (size_t)GEMV_STAGES * 2 * T * GEMV_BOX + (size_t)16 * T * G * 2 + 8 + 2 * GEMV_STAGES * 8;
-}
-
-template <int T>
-static int launch_t(const CUtensorMap& map, const uint16_t* x, const uint16_t* scales, uint16_t* y, int m, int n,
-                    int k, int group, int ntiles, int ncta, cudaStream_t stream) {
+static int launch_t(const uint8_t* codes, const CUtensorMap& xmap, const uint16_t* scales, uint16_t* y, int m,
+                    int n, int k, int group, int ntiles, int ncta, cudaStream_t stream, const char* who) {
     static int configured_smem[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
-    const size_t smem = gemv_smem_bytes<T>(k / group);
-    if (dev < 64 && (size_t)configured_smem[dev] < smem) {
+    if (dev >= 64) dev = 63;
+    const int G = k / group;
+    const size_t stage = ((size_t)GemvStage<T>::bytes(m) + 1023) & ~size_t(1023);
+    const size_t fixed = 1024 + (size_t)8 * T * G * 8 + GEMV_MAX_STAGES * 16;
+    int nstages = GEMV_MAX_STAGES;
+    while (nstages > 2 && fixed + nstages * stage > (size_t)GEMV_SMEM_LIMIT) nstages--;
+    const size_t smem = fixed + nstages * stage;
+    if (smem > (size_t)GEMV_SMEM_LIMIT) return fail(BQ_ERR_INVALID, "%s: shape needs too much shared memory", who);
+    if ((size_t)configured_smem[dev] < smem) {
         if (cudaFuncSetAttribute(q2_gemv_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
-            return fail(BQ_ERR_LAUNCH, "q2 gemv: cannot reserve %zu bytes of shared memory", smem);
+            return fail(BQ_ERR_LAUNCH, "%s: cannot reserve %zu bytes of shared memory", who, smem);
         configured_smem[dev] = (int)smem;
     }
-    q2_gemv_kernel<T><<<ncta, GEMV_THREADS, smem, stream>>>(map, x, scales, y, m, n, k, group, ntiles);
+    // codes boxes of exactly T and T-1 tiles of rows (CTAs get one or the other)
+    CUtensorMap map_full, map_less;
+    int st = make_tmap_2d_u8(&map_full, codes, k / 4, n, k / 4, 128, 16 * T, true, who);
+    if (st) return st;
+    if ((st = make_tmap_2d_u8(&map_less, codes, k / 4, n, k / 4, 128, T > 1 ? 16 * (T - 1) : 16, true, who))) return st;
+    q2_gemv_kernel<T><<<ncta, GEMV_THREADS, smem, stream>>>(map_full, map_less, xmap, scales, y, m, n, k, group,
+                                                            ntiles, nstages);
     return BQ_OK;
 }
 
@@ -277,30 +349,31 @@ int launch_q2_gemv(const uint16_t* x, const bq_q2_weight* w, uint16_t* y, uint32
     const int G = (int)(w->k / w->group);
     const int ntiles = (int)((w->n + 15) / 16);
     int tmax = GEMV_MAX_T;
-    while (tmax > 1 && (size_t)16 * tmax * G * 2 > (size_t)GEMV_MAX_SCALE_BYTES) tmax--;
-    if ((size_t)16 * tmax * G * 2 > (size_t)GEMV_MAX_SCALE_BYTES)
+    while (tmax > 1 && (size_t)64 * tmax * G > 96 * 1024) tmax--;
+    if ((size_t)64 * tmax * G > 96 * 1024)
         return fail(BQ_ERR_INVALID, "%s: k/group = %d groups per row is too many", who, G);
     int ncta = ntiles < sm_count() ? ntiles : sm_count();
     int T = (ntiles + ncta - 1) / ncta;
     if (T > tmax) {
-        T = tmax;
-        ncta = (ntiles + T - 1) / T;
+        ncta = (ntiles + tmax - 1) / tmax;
+        T = (ntiles + ncta - 1) / ncta;  // every CTA then gets T or T - 1 tiles
     }
     const uint8_t* codes = (const uint8_t*)w->data;
     const uint16_t* scales = (const uint16_t*)(codes + (size_t)w->n * (w->k / 4));
-    CUtensorMap map;
-    int st = make_tmap_2d_u8(&map, codes, w->k / 4, w->n, w->k / 4, 128, 16, true, who);
+    CUtensorMap xmap;
+    // activations x [m][k] as 16-bit elements, boxes of 256 columns x m rows
+    int st = make_tmap_2d(&xmap, x, 2, w->k, m, (uint64_t)w->k * 2, GEMV_XBOX, m, false, who);
     if (st) return st;
     const int mm = (int)m, n = (int)w->n, k = (int)w->k, gr = (int)w->group;
     switch (T) {
-        case 1: st = launch_t<1>(map, x, scales, y, mm, n, k, gr, ntiles, ncta, stream); break;
-        case 2: st = launch_t<2>(map, x, scales, y, mm, n, k, gr, ntiles, ncta, stream); break;
-        case 3: st = launch_t<3>(map, x, scales, y, mm, n, k, gr, ntiles, ncta, stream); break;
-        case 4: st = launch_t<4>(map, x, scales, y, mm, n, k, gr, ntiles, ncta, stream); break;
-        case 5: st = launch_t<5>(map, x, scales, y, mm, n, k, gr, ntiles, ncta, stream); break;
-        case 6: st = launch_t<6>(map, x, scales, y, mm, n, k, gr, ntiles, ncta, stream); break;
-        case 7: st = launch_t<7>(map, x, scales, y, mm, n, k, gr, ntiles, ncta, stream); break;
-        case 8: st = launch_t<8>(map, x, scales, y, mm, n, k, gr, ntiles, ncta, stream); break;
+        case 1: st = launch_t<1>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
+        case 2: st = launch_t<2>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
+        case 3: st = launch_t<3>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
+        case 4: st = launch_t<4>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
+        case 5: st = launch_t<5>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
+        case 6: st = launch_t<6>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
+        case 7: st = launch_t<7>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
+        case 8: st = launch_t<8>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
         default: return fail(BQ_ERR_INVALID, "%s: internal tile count %d", who, T);
     }
     if (st) return st;

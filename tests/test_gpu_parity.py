@@ -296,3 +296,51 @@ def test_q2_mmq_prefill_full(B, m):
     yv = (y[rows].astype(np.uint32) << 16).view(np.float32)
     rel = np.linalg.norm(yv - yd) / np.linalg.norm(yd)
     assert rel < 1e-2
+
+
+# ------------------------------------------------------------------------------ Q4_K MMQ
+@pytest.mark.parametrize("m,n,k", [(1, 8, 256), (5, 37, 512), (130, 300, 1024), (257, 129, 768), (64, 1000, 2048)])
+def test_q4k_mmq_small(B, m, n, k):
+    d = synth.small_dense(800 + m + n, n, k, m)
+    wq = B.quantize_weight_q4k(to_dev_u16_as_bf16(d["w"]))
+    act = B.quantize_act_q8_1(to_dev_u16_as_bf16(d["x"]))
+    y = bf16_dev_to_u16(B.q4k_mmq_gemm(act, wq, m, n, k))
+    ref = O.q4k_mmq(O.quantize_q8_1(d["x"]), O.quantize_q4k(d["w"]), m, n, k)
+    check_bf16_vs_f64(y, ref, "q4k mmq m=%d n=%d k=%d" % (m, n, k))
+
+
+def test_q4k_ffn_prefill_full(B):
+    """The FFN prefill at m = 2048 (gate and up MMQ, SiLU*mul, q8_1 of h, down MMQ).
+    Gate and up are checked on sampled rows against the oracle on the same q8_1 input; the
+    down GEMM is checked at its full k = 17408 on the oracle's own h for those rows (uploaded
+    and quantised on the GPU, bit-exact); the kernel chain's own output is compared loosely
+    with the oracle chain (a sanity check: the two h differ by BF16 rounding)."""
+    import torch
+    d = synth.q4k_ffn_prefill()
+    m, hidden, inter = d["m"], d["hidden"], d["inter"]
+    wq = {kk: B.quantize_weight_q4k(to_dev_u16_as_bf16(d[kk])) for kk in ("w_gate", "w_up", "w_down")}
+    wq_ref = {kk: O.quantize_q4k(d[kk]) for kk in ("w_gate", "w_up", "w_down")}
+    for kk in wq:
+        assert np.array_equal(u8_dev(wq[kk]), wq_ref[kk]), kk
+    a1 = B.quantize_act_q8_1(to_dev_u16_as_bf16(d["x"]))
+    a1_ref = O.quantize_q8_1(d["x"])
+    assert np.array_equal(u8_dev(a1), a1_ref)
+    gt = B.q4k_mmq_gemm(a1, wq["w_gate"], m, inter, hidden)
+    ut = B.q4k_mmq_gemm(a1, wq["w_up"], m, inter, hidden)
+    h = B.silu_mul_bf16(gt, ut)
+    out = B.q4k_mmq_gemm(B.quantize_act_q8_1(h), wq["w_down"], m, hidden, inter)
+    rows = np.unique(np.concatenate([np.random.default_rng(5).choice(m, 14, replace=False), [0, m - 1]]))
+    g_ref = O.q4k_mmq(a1_ref, wq_ref["w_gate"], m, inter, hidden, rows=rows)
+    u_ref = O.q4k_mmq(a1_ref, wq_ref["w_up"], m, inter, hidden, rows=rows)
+    check_bf16_vs_f64(bf16_dev_to_u16(gt)[rows], g_ref, "q4k gate")
+    check_bf16_vs_f64(bf16_dev_to_u16(ut)[rows], u_ref, "q4k up")
+    # oracle chain for the sampled rows: BF16 g, u -> BF16 h -> q8_1 -> down
+    h_ref = O.silu_mul_bf16(O.f64_to_bf16(g_ref), O.f64_to_bf16(u_ref))
+    a2_ref = O.quantize_q8_1(h_ref)
+    y_ref = O.q4k_mmq(a2_ref, wq_ref["w_down"], len(rows), hidden, inter)
+    a2 = B.quantize_act_q8_1(to_dev_u16_as_bf16(h_ref))
+    assert np.array_equal(u8_dev(a2), a2_ref)
+    y_down = bf16_dev_to_u16(B.q4k_mmq_gemm(a2, wq["w_down"], len(rows), hidden, inter))
+    check_bf16_vs_f64(y_down, y_ref, "q4k down (k=17408)")
+    yv = (bf16_dev_to_u16(out)[rows].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert np.linalg.norm(yv - y_ref) / np.linalg.norm(y_ref) < 1e-2
