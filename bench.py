@@ -270,21 +270,14 @@ def run_ours(args, rank, local, world):
     alg_bytes = wbytes + (K_HIDDEN * 2 + N_QKVZ * 2) * (1 + 4) / 2.0  # + x and y, averaged over m=1 and m=4
     achieved = alg_bytes / per_launch / 1e9
 
-    # kernel-only per-launch durations (event-bracketed single launches, not graphed)
-    def one(i, m):
-        (B.q2_gemv if m == 1 else B.q2_gemv_batchm)(x1 if m == 1 else x4, layers[i % L],
-                                                    out=(y1 if m == 1 else y4)[i % L])
+    # per-m launch times: a graph of the L launches at one m, so host launch overhead is out
     kern = {}
     for m in (1, 4):
-        ts = []
-        for i in range(40):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            one(i, m)
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b) / 1e3)
-        kern["m%d" % m] = {"us": statistics.median(ts) * 1e6, "weight_GBps": wbytes / statistics.median(ts) / 1e9}
+        gm = _graph(lambda: [(B.q2_gemv(x1, layers[i], out=y1[i]) if m == 1 else
+                              B.q2_gemv_batchm(x4, layers[i], out=y4[i])) for i in range(L)])
+        t = _time_graph(gm, max(3, args.steps // 4)) / L
+        kern["m%d" % m] = {"us_per_launch": round(t * 1e6, 3), "weight_GBps": round(wbytes / t / 1e9, 1)}
+        del gm
 
     # ---- e2e through the public API: x from pinned host memory, all outputs back to host
     x1h = x1.cpu().pin_memory()
@@ -329,7 +322,7 @@ def run_ours(args, rank, local, world):
                      "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
                      "kernel": "q2_gemv_kernel", "peak_source": peak_src,
                      "note": "algorithmic bytes per launch (weight + x + y) / (graph elapsed / launches)"},
-        "kernel_only": kern,
+        "per_m": kern,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
