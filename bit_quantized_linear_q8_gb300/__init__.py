@@ -17,7 +17,7 @@ from ._abi import BQ8Error, LibraryNotBuilt, check, lib  # noqa: F401
 
 __all__ = [
     "Q2Weight", "q2_pack", "quantize_weight_q4k", "quantize_act_q8_1", "q2_gemv", "q2_gemv_batchm",
-    "silu_mul_bf16", "ffn_q2_km", "q2_mmq_gemm", "q4k_mmq_gemm", "dequant_q2_to_bf16", "q2_prefill_proj",
+    "silu_mul_bf16", "ffn_q2_km", "ffn_q2_km_noalloc", "q2_mmq_gemm", "q4k_mmq_gemm", "dequant_q2_to_bf16", "q2_prefill_proj",
     "q2_weight_bytes", "q8_1_bytes", "q4k_weight_bytes", "BQ8Error", "LibraryNotBuilt",
 ]
 
@@ -155,6 +155,22 @@ def ffn_q2_km(x, gate: Q2Weight, up: Q2Weight, down: Q2Weight, gate_scratch=None
     check(lib().ffn_q2_km(_ptr(x), ctypes.byref(dg), ctypes.byref(du), ctypes.byref(dd), _ptr(gate_scratch),
                           _ptr(up_scratch), _ptr(out), m, _stream()))
     return out, gate_scratch, up_scratch
+
+
+def ffn_q2_km_noalloc(x, gate: Q2Weight, up: Q2Weight, down: Q2Weight, out=None):
+    """ffn_q2_km with its two intermediates in the library's built-in device array (for
+    callers that cannot allocate; m * inter <= 262144).  Calls that overlap on the GPU race
+    on that array.  Returns out [m, hidden]."""
+    torch = _torch()
+    m = x.shape[0]
+    _need(x, torch.bfloat16, "x", (m, gate.k))
+    if out is None:
+        out = torch.empty((m, gate.k), dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, "out", (m, gate.k))
+    dg, du, dd = gate.desc(), up.desc(), down.desc()
+    check(lib().ffn_q2_km_noalloc(_ptr(x), ctypes.byref(dg), ctypes.byref(du), ctypes.byref(dd), _ptr(out), m,
+                                  _stream()))
+    return out
 
 
 def q2_mmq_gemm(act_q8, w: Q2Weight, m: int, out=None):

@@ -37,6 +37,7 @@ SIGNATURES = {
     "q2_gemv_batchm": (I, [P, WD, P, U32, P]),
     "silu_mul_bf16": (I, [P, P, P, SZ, P]),
     "ffn_q2_km": (I, [P, WD, WD, WD, P, P, P, U32, P]),
+    "ffn_q2_km_noalloc": (I, [P, WD, WD, WD, P, U32, P]),
     "q2_mmq_gemm": (I, [P, WD, P, U32, P]),
     "q4k_mmq_gemm": (I, [P, P, P, U32, U32, U32, P]),
     "dequant_q2_to_bf16": (I, [WD, P, P]),

@@ -123,6 +123,28 @@ int silu_mul_bf16(const uint16_t* gate, const uint16_t* up, uint16_t* out, size_
 int ffn_q2_km(const uint16_t* x, const bq_q2_weight* gate, const bq_q2_weight* up, const bq_q2_weight* down,
               uint16_t* gate_scratch, uint16_t* up_scratch, uint16_t* out, uint32_t m, bq_stream_t stream);
 
+/* Largest m * inter that ffn_q2_km_noalloc accepts (values per intermediate buffer). */
+#define BQ_FFN_NOALLOC_MAX_ELEMS 262144u
+
+/* ffn_q2_km for callers that cannot allocate device memory (no counterpart on the pages:
+ * it exists for this library's users).  A host framework that hands a plugin only its
+ * inputs and outputs, a runtime whose pool owns all device memory, or C code linked
+ * without an allocator has nowhere to put ffn_q2_km's two [m][inter] intermediates; this
+ * entry point keeps them in a fixed 1 MiB array inside the library's device image and calls
+ * no allocator at all.  Same arguments and result as ffn_q2_km without the two scratch
+ * pointers; out = SiLU(x @ gate^T) * (x @ up^T) @ down^T, [m][hidden] BF16.
+ *  - m * inter must not exceed BQ_FFN_NOALLOC_MAX_ELEMS (else BQ_ERR_INVALID, nothing
+ *    launched); every other check is ffn_q2_km's.
+ *  - The first call on each device looks up the array's device address with that device
+ *    current (cudaGetSymbolAddress) and caches it; make that first call before any stream
+ *    capture on the device.
+ *  - The array is shared by every call in the process and keeps the last call's contents;
+ *    calls that overlap on the GPU (other streams or host threads) race on it.  Calls on
+ *    one stream are ordered and safe.  The array stays allocated on every GPU that loaded
+ *    the library until the process exits. */
+int ffn_q2_km_noalloc(const uint16_t* x, const bq_q2_weight* gate, const bq_q2_weight* up, const bq_q2_weight* down,
+                      uint16_t* out, uint32_t m, bq_stream_t stream);
+
 /* Q2_0 MMQ: out[m][n] = q8_1(act) @ Wdq^T with integer products per 32-value block and
  * fp32 rescaling, BF16 store.  act_q8 is quantize_act_q8_1's output for [m][w->k];
  * w->group must be 128 (the page's MMQ condition).  Any m >= 1 and any n.
