@@ -346,38 +346,7 @@ int launch_q2_gemv(const uint16_t* x, const bq_q2_weight* w, uint16_t* y, uint32
             return fail(BQ_ERR_LAUNCH, "%s: memset failed", who);
         return ok();
     }
-    const int G = (int)(w->k / w->group);
-    const int ntiles = (int)((w->n + 15) / 16);
-    int tmax = GEMV_MAX_T;
-    while (tmax > 1 && (size_t)64 * tmax * G > 96 * 1024) tmax--;
-    if ((size_t)64 * tmax * G > 96 * 1024)
-        return fail(BQ_ERR_INVALID, "%s: k/group = %d groups per row is too many", who, G);
-    int ncta = ntiles < sm_count() ? ntiles : sm_count();
-    int T = (ntiles + ncta - 1) / ncta;
-    if (T > tmax) {
-        ncta = (ntiles + tmax - 1) / tmax;
-        T = (ntiles + ncta - 1) / ncta;  // every CTA then gets T or T - 1 tiles
-    }
-    const uint8_t* codes = (const uint8_t*)w->data;
-    const uint16_t* scales = (const uint16_t*)(codes + (size_t)w->n * (w->k / 4));
-    CUtensorMap xmap;
-    // activations x [m][k] as 16-bit elements, boxes of 256 columns x m rows
-    int st = make_tmap_2d(&xmap, x, 2, w->k, m, (uint64_t)w->k * 2, GEMV_XBOX, m, false, who);
-    if (st) return st;
-    const int mm = (int)m, n = (int)w->n, k = (int)w->k, gr = (int)w->group;
-    switch (T) {
-        case 1: st = launch_t<1>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
-        case 2: st = launch_t<2>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
-        case 3: st = launch_t<3>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
-        case 4: st = launch_t<4>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
-        case 5: st = launch_t<5>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
-        case 6: st = launch_t<6>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
-        case 7: st = launch_t<7>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
-        case 8: st = launch_t<8>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
-        default: return fail(BQ_ERR_INVALID, "%s: internal tile count %d", who, T);
-    }
-    if (st) return st;
-    return check_launch(who);
+    return launch_q2_gemv_tc(x, w, y, m, stream, who);
 }
 
 static int check_gemv_args(const uint16_t* x, const bq_q2_weight* w, const uint16_t* y, uint32_t m, const char* who) {

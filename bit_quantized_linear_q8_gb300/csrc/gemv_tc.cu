@@ -7,23 +7,30 @@
 // consume ~176 K weights per microsecond per SM.  Design (GB300, sm_103a):
 //
 //  * Weights are the MMA's A operand (M = 128 rows), held in tensor memory.  Eight
-//    "unpack" warps turn each 2-bit code into the mantissa of BF16 1.0 with one lop3 per
-//    pair of codes, v = 1 + c*s (s = 2^-7, 2^-5, 2^-3, 2^-3 by the code's bit position),
-//    and store the rows into TMEM with tcgen05.st (lane = row).
+//    "unpack" warps mask each pair of 2-bit codes straight into the mantissa bits of a
+//    BF16 pair with exponent field 0: a subnormal of value c * 2^(p - 133), p = 0, 2 or 4
+//    by the code's bit position (one AND per pair, a shift for the other positions), and
+//    store the rows into TMEM with tcgen05.st (lane = row).  The tensor cores take BF16
+//    subnormals exactly.
 //  * Activations are the B operand (N = 16; only rows 0..m-1 matter, the descriptor's
-//    row-group stride of 0 repeats rows 0..7 for 8..15): per 128-column group the unpack
-//    warps write a K-major tile of x/s, permuted into the order of the TMEM columns.
-//  * sum_k (1 + c s) x/s = sum x/s + sum c x, so the wanted sum_k (c - 2) x is the MMA row
-//    minus the row of a virtual weight with every code 2.  TMEM lane 31 of each 32-lane
-//    quadrant is that row (so a CTA holds 4 x 31 = 124 weight rows); the epilogue takes
-//    the difference with one shuffle and applies the group's BF16 scale d in fp32.
+//    row-group stride of 0 repeats rows 0..7 for 8..15): per 128-column group four
+//    epilogue warps write a K-major tile of x * 2^(69 - p), permuted into the order of the
+//    TMEM columns, so every product is c * x * 2^-64 exactly.
+//  * The wanted sum_k (c - 2) x * 2^-64 is the MMA row minus the row of a virtual weight
+//    with every code 2.  TMEM lane 31 of each 32-lane quadrant is that row (so a CTA holds
+//    4 x 31 = 124 weight rows); the epilogue warps take the difference with one shuffle,
+//    apply the group's BF16 scale d in fp32 and the factor 2^64 at the store.
 //  * One tcgen05.mma (128 x 16 x 16) per 16 columns.  Its issue costs the issuing thread
-//    about 54 cycles, so four issuing warps take the 128-column groups round robin, each
-//    with its own A/B/D buffer, and commit to an mbarrier the epilogue waits on.
+//    about 54 cycles, so five issuing warps take the 128-column groups round robin and
+//    commit to per-accumulator mbarriers.  The unpack warps fill TMEM a pair of groups at a
+//    time (three A blocks of two groups), the epilogue warps build B tiles and drain
+//    accumulators four groups (one TMA stage) at a time, so the fixed cost of every wait,
+//    fence and arrival is paid once per pair or per stage (eight accumulators / B tiles).
 //  * A producer warp streams the CTA's rows through a 5-stage TMA ring (512 columns per
-//    stage, 128-byte swizzle) plus the stage's activation columns.  The weights do not
-//    depend on the previous kernel, so their copies are issued before
-//    griddepcontrol.wait (programmatic dependent launch); the activations after it.
+//    stage, 128-byte swizzle) plus the stage's activation columns, and bulk-copies the
+//    rows' group scales.  The weights do not depend on the previous kernel, so their
+//    copies are issued before griddepcontrol.wait (programmatic dependent launch); the
+//    activations after it.
 //  * Shapes with few rows split K over a thread-block cluster of up to 8 CTAs; the partial
 //    sums meet in the leader CTA through distributed shared memory.
 //  * Every mbarrier wait is bounded; on a timeout the kernel records it in the status word
@@ -32,21 +39,27 @@
 
 namespace bq8 {
 
-constexpr int TC_UW = 8;                              // unpack / B-tile / epilogue warps
-constexpr int TC_IW = 4;                              // MMA-issuing warps
-constexpr int TC_THREADS = (TC_UW + TC_IW + 1) * 32;  // + one TMA producer warp
-constexpr int TC_PRODUCER = TC_UW + TC_IW;            // warp index of the producer
-constexpr int TC_NA = TC_IW;                          // A/B/D buffers: issuer i owns buffer i
-constexpr int TC_NS = 5;                              // TMA stages, 4 groups (512 columns) each
-constexpr int TC_RQ = 31;                             // weight rows per TMEM lane quadrant
-constexpr int TC_ROWS = 4 * TC_RQ;                    // 124 weight rows per CTA
-constexpr int TC_CODES = 16384;                       // stage codes: <= 124 rows x 128 B
-constexpr int TC_XB = 8192;                           // stage activations: 2 boxes x m x 256 bf16
+constexpr int TC_UW = 8;                             // unpack warps 0..7 (two per TMEM lane quadrant)
+constexpr int TC_EW = 4;                             // epilogue / B-tile warps 8..11 (one per quadrant)
+constexpr int TC_IW = 5;                             // MMA-issuing warps 12..16
+constexpr int TC_EW0 = TC_UW;
+constexpr int TC_IW0 = TC_UW + TC_EW;
+constexpr int TC_PRODUCER = TC_IW0 + TC_IW;          // warp 17: TMA producer
+constexpr int TC_THREADS = (TC_PRODUCER + 1) * 32;
+constexpr int TC_NAB = 3;                            // A blocks of two groups (128 TMEM columns)
+constexpr int TC_ND = 8;                             // D accumulators and B tiles
+constexpr int TC_NS = 5;                             // TMA stages, 4 groups (512 columns) each
+constexpr int TC_RQ = 31;                            // weight rows per TMEM lane quadrant
+constexpr int TC_ROWS = 4 * TC_RQ;                   // 124 weight rows per CTA
+constexpr int TC_CODES = 16384;                      // stage codes: <= 124 rows x 128 B
+constexpr int TC_XB = 8192;                          // stage activations: 2 boxes x m x 256 bf16
 constexpr int TC_STAGE = TC_CODES + TC_XB;
-constexpr int TC_BT = 2048;                           // B tile: 8 rows x 128 bf16 (K-major)
+constexpr int TC_LBO = 144;                          // B core matrices along K, padded (no bank conflicts)
+constexpr int TC_BT = 16 * TC_LBO;                   // B tile: 8 rows x 128 bf16 (K-major)
 constexpr int TC_TMEM_COLS = 512;
-constexpr int TC_ACOL = 0;                            // A buffer a: TMEM columns 64a .. 64a + 63
-constexpr int TC_DCOL = 256;                          // D buffer a: TMEM columns 256 + 16a ..
+constexpr int TC_ACOL = 0;                           // A block b: TMEM columns 128b .. 128b + 127
+constexpr int TC_DCOL = 128 * TC_NAB;                // D accumulator d: TMEM columns 384 + 16d ..
+constexpr int TC_NBAR = 2 * TC_NS + TC_NAB + 2 * TC_ND + 1;
 constexpr int TC_SMEM_LIMIT = 225 * 1024;
 
 static __device__ unsigned int g_gemv_tc_status;
@@ -130,40 +143,55 @@ __device__ __forceinline__ float ld_cluster_f32(const void* local, uint32_t rank
 // The 32 TMEM columns (64 weights) of one unpack thread for one group: four 32-bit words
 // of packed codes (word w holds bytes 4w..4w+3 of the row's 32-byte pack block, byte l
 // carrying columns 32i + l of sub-blocks i = 0..3 in bits 2i).  Column 8w' + 2i + h holds
-// the pair (columns 32i + 4w + h, 32i + 4w + h + 2) for h = 0, 1.
+// the pair (columns 32i + 4w + h, 32i + 4w + h + 2) for h = 0, 1 as BF16 subnormals
+// c * 2^(p_i - 133), p = 0, 2, 4, 4 for i = 0..3.
 __device__ __forceinline__ void unpack_group(const uint4& cw, uint32_t (&r)[32]) {
-    const uint32_t one = 0x3F803F80u, m0 = 0x00030003u, m1 = 0x000C000Cu, m2 = 0x00300030u;
     const uint32_t wds[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
     for (int q = 0; q < 4; q++) {
         const uint32_t w = wds[q], s2 = w >> 2, s8 = w >> 8, s10 = w >> 10;
-        r[8 * q + 0] = and_or(w, m0, one);
-        r[8 * q + 1] = and_or(s8, m0, one);
-        r[8 * q + 2] = and_or(w, m1, one);
-        r[8 * q + 3] = and_or(s8, m1, one);
-        r[8 * q + 4] = and_or(w, m2, one);
-        r[8 * q + 5] = and_or(s8, m2, one);
-        r[8 * q + 6] = and_or(s2, m2, one);
-        r[8 * q + 7] = and_or(s10, m2, one);
+        r[8 * q + 0] = w & 0x00030003u;
+        r[8 * q + 1] = s8 & 0x00030003u;
+        r[8 * q + 2] = w & 0x000C000Cu;
+        r[8 * q + 3] = s8 & 0x000C000Cu;
+        r[8 * q + 4] = w & 0x00300030u;
+        r[8 * q + 5] = s8 & 0x00300030u;
+        r[8 * q + 6] = s2 & 0x00300030u;
+        r[8 * q + 7] = s10 & 0x00300030u;
     }
 }
 
+__device__ __forceinline__ void tc_ld8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 8; j++) v[j] = __uint_as_float(r[j]);
+}
+
+template <int MV>  // activation rows m
 __global__ void __launch_bounds__(TC_THREADS, 1)
     q2_gemv_tc_kernel(const __grid_constant__ CUtensorMap cmap_hi, const __grid_constant__ CUtensorMap cmap_lo,
-                      const __grid_constant__ CUtensorMap xmap, const uint16_t* __restrict__ scales,
-                      uint16_t* __restrict__ y, int m, int n, int k, int group, int nclus, int csplit, int rows_hi,
-                      int ngmax) {
+                      const __grid_constant__ CUtensorMap xmap, const uint8_t* __restrict__ splane,
+                      uint16_t* __restrict__ y, int n, int k, int group, int nclus, int csplit, int rows_hi,
+                      int sc_cap) {
+    constexpr int m = MV;
+    constexpr int DW = MV > 4 ? 8 : 4;  // accumulator columns read per group
     extern __shared__ uint8_t smem_raw[];
     uint8_t* stages = align1024(smem_raw);
     uint8_t* btile = stages + TC_NS * TC_STAGE;
-    float* red = reinterpret_cast<float*>(btile + TC_NA * TC_BT);   // [8][124] partial sums
-    uint16_t* sc = reinterpret_cast<uint16_t*>(red + 8 * TC_ROWS);  // [ngmax][124] scales
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sc + ((ngmax * TC_ROWS + 7) & ~7));
-    uint64_t* full = bars;               // TMA stage landed (1 arrival + bytes)
-    uint64_t* empty = bars + TC_NS;      // stage consumed (one arrival per unpack warp)
-    uint64_t* afull = bars + 2 * TC_NS;  // A/B buffer written (one arrival per unpack warp)
-    uint64_t* mdone = afull + TC_NA;     // MMAs of the buffer's group complete (commit)
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mdone + TC_NA);
+    float* red = reinterpret_cast<float*>(btile + TC_ND * TC_BT);  // [8][124] partial sums
+    uint8_t* scs = reinterpret_cast<uint8_t*>(red + 8 * TC_ROWS);   // the rows' scale bytes
+    uint64_t* full = reinterpret_cast<uint64_t*>(scs + sc_cap);     // TMA stage landed
+    uint64_t* empty = full + TC_NS;                                  // stage consumed
+    uint64_t* afull = empty + TC_NS;                                 // A block written
+    uint64_t* bfull = afull + TC_NAB;                                // B tile written, accumulator read
+    uint64_t* mdone = bfull + TC_ND;                                 // accumulator's MMAs complete
+    uint64_t* sfull = mdone + TC_ND;                                 // scales landed
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sfull + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NG = k >> 7;
@@ -175,58 +203,50 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int NGc = (int)((int64_t)(rank + 1) * NG / csplit) - gb;
     const int nst = (NGc + 3) >> 2;
     const int G = k / group;
-    const uint32_t xbytes = 2u * (uint32_t)m * 256u * 2u;
+    const uint32_t xbytes = 1024u * (uint32_t)m;  // two boxes of m rows x 256 BF16
     const CUtensorMap* cmap = R == rows_hi ? &cmap_hi : &cmap_lo;
+    // scale bytes of the CTA's rows: [s_lo, s_hi) arrive by one bulk copy, the rest (at most
+    // 14 bytes at the end of the plane) is copied by the threads that own those rows
+    const int64_t s_lo = ((int64_t)r0 * G * 2) & ~int64_t(15);
+    int64_t s_hi = ((int64_t)(r0 + R) * G * 2 + 15) & ~int64_t(15);
+    const int64_t plane16 = ((int64_t)n * G * 2) & ~int64_t(15);
+    if (s_hi > plane16) s_hi = plane16;
+    if (s_hi < s_lo) s_hi = s_lo;
+    const uint32_t sbytes = (uint32_t)(s_hi - s_lo);
     bool failed = false;
+    float tot[MV];
+#pragma unroll
+    for (int j = 0; j < MV; j++) tot[j] = 0.f;
 
     if (warp == TC_PRODUCER && lane == 0) {
         for (int s = 0; s < TC_NS; s++) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], TC_UW);
+            mbar_init(&empty[s], TC_UW + TC_EW);
         }
-        for (int a = 0; a < TC_NA; a++) {
-            mbar_init(&afull[a], TC_UW);
-            mbar_init(&mdone[a], 1);
+        for (int b = 0; b < TC_NAB; b++) mbar_init(&afull[b], TC_UW);
+        for (int d = 0; d < TC_ND; d++) {
+            mbar_init(&bfull[d], TC_EW);
+            mbar_init(&mdone[d], 1);
         }
+        mbar_init(sfull, 1);
         fence_barrier_init();
         // weights first: they do not depend on the kernel before this one
+        mbar_arrive_expect_tx(sfull, sbytes);
+        if (sbytes) bulk_load(scs, splane + s_lo, sbytes, sfull);
         for (int st = 0; st < TC_NS && st < nst; st++) {
             mbar_arrive_expect_tx(&full[st], (uint32_t)R * 128u + xbytes);
             tma_load_2d(stages + st * TC_STAGE, cmap, (gb + 4 * st) * 32, r0, &full[st]);
         }
     }
-    if (warp == TC_UW) {  // tensor memory for the A and D buffers
+    if (warp == TC_IW0) {  // tensor memory for the A blocks and the accumulators
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
                      "n"(TC_TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-    }
-    if (warp < TC_UW) {  // this CTA's group scales, sc[group][row]; eight loads in flight per thread
-        const int total = R * NGc;
-        for (int base = threadIdx.x; base < total; base += 8 * TC_UW * 32) {
-            uint16_t v[8];
-#pragma unroll
-            for (int u = 0; u < 8; u++) {
-                const int e = base + u * TC_UW * 32;
-                const int row = e / NGc, gl = e - row * NGc;
-                v[u] = e < total ? __ldg(scales + (size_t)(r0 + row) * G + ((gb + gl) * 128) / group) : (uint16_t)0;
-            }
-#pragma unroll
-            for (int u = 0; u < 8; u++) {
-                const int e = base + u * TC_UW * 32;
-                const int row = e / NGc, gl = e - row * NGc;
-                if (e < total) sc[gl * TC_ROWS + row] = v[u];
-            }
-        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tslot;
-
-    float tot[4] = {0.f, 0.f, 0.f, 0.f};
-    const int qd = warp & 3, hh = (warp >> 2) & 1;
-    const int rho = TC_RQ * qd + lane;  // weight row of an unpack thread (lane < 31)
-    const uint32_t tq = tbase + ((uint32_t)(32 * qd) << 16);
 
     if (warp == TC_PRODUCER) {
         if (lane == 0) {
@@ -247,91 +267,170 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 tma_load_2d(xs + m * 512, &xmap, (gb + 4 * st) * 128 + 256, 0, &full[s]);
             }
         }
-    } else if (warp >= TC_UW) {  // MMA issuers: issuer i owns buffer i and groups i, i + 4, ...
-        const int iw = warp - TC_UW;
+    } else if (warp >= TC_IW0) {  // MMA issuers: issuer i takes groups i, i + 5, ...
+        const int iw = warp - TC_IW0;
         if (lane == 0) {
-            const uint32_t bbase = smem_u32(btile + iw * TC_BT);
-            const uint32_t dcol = tbase + TC_DCOL + 16 * iw, acol = tbase + TC_ACOL + 64 * iw;
             int last = -1;
             for (int gi = iw; gi < NGc; gi += TC_IW) {
-                if (!mbar_wait(&afull[iw], (gi / TC_NA) & 1)) {
+                const int d = gi % TC_ND, pr = gi >> 1, b = pr % TC_NAB;
+                if (!mbar_wait(&afull[b], (pr / TC_NAB) & 1) || !mbar_wait(&bfull[d], (gi / TC_ND) & 1)) {
                     failed = true;
                     break;
                 }
                 tc_fence_after();
+                const uint32_t bb = smem_u32(btile + d * TC_BT), dcol = tbase + TC_DCOL + 16 * d;
+                const uint32_t acol = tbase + TC_ACOL + 128 * b + 64 * (gi & 1);
 #pragma unroll
-                for (int kk = 0; kk < 8; kk++) tc_mma(dcol, acol + 8 * kk, smem_desc(bbase + 256 * kk, 128, 0), kk > 0);
-                tc_commit(&mdone[iw]);
+                for (int kk = 0; kk < 8; kk++)
+                    tc_mma(dcol, acol + 8 * kk, smem_desc(bb + 2 * TC_LBO * kk, TC_LBO, 0), kk > 0);
+                tc_commit(&mdone[d]);
                 last = gi;
             }
-            // the buffer's last commit must land before the tensor memory is released
-            if (last >= 0 && !mbar_wait(&mdone[iw], (last / TC_NA) & 1)) failed = true;
+            // the last commit must land before the tensor memory is released
+            if (last >= 0 && !mbar_wait(&mdone[last % TC_ND], (last / TC_ND) & 1)) failed = true;
         }
-    } else {  // unpack warps
-        auto epilogue = [&](int ge) {
-            const int a = ge % TC_NA;
-            if (4 * hh < m) {  // warp-uniform
-                float d4[4];
-                tc_ld4(tq + TC_DCOL + 16 * a + 4 * hh, d4);
-                const float d = bf16_bits_to_f32(sc[ge * TC_ROWS + (lane < TC_RQ ? rho : 0)]);
-#pragma unroll
-                for (int j = 0; j < 4; j++) {
-                    const float off = __shfl_sync(0xffffffffu, d4[j], 31);
-                    tot[j] = fmaf(d, d4[j] - off, tot[j]);
-                }
-            }
-        };
-        for (int gi = 0; gi < NGc; gi++) {
-            const int a = gi % TC_NA, st = gi >> 2, s = st % TC_NS, gl = gi & 3;
-            if (gl == 0 && !mbar_wait(&full[s], (st / TC_NS) & 1)) {
+    } else if (warp >= TC_EW0) {  // epilogue warps: per stage, B tiles out, accumulators of two stages back in
+        const int qd = warp & 3;
+        const int rho = TC_RQ * qd + lane;
+        const bool rowok = lane < TC_RQ && rho < R;
+        const int64_t srow = (int64_t)(r0 + (rowok ? rho : 0)) * G * 2;  // the row's scales in the plane
+        const uint32_t tq = tbase + ((uint32_t)(32 * qd) << 16);
+        if (rowok) {  // scale bytes past the bulk copy: this thread's own row only
+            for (int64_t o = srow > s_hi ? srow : s_hi; o < srow + (int64_t)G * 2; o += 2)
+                *reinterpret_cast<uint16_t*>(scs + (o - s_lo)) = __ldg(reinterpret_cast<const uint16_t*>(splane + o));
+        }
+        const uint16_t* myscale = reinterpret_cast<const uint16_t*>(scs + (srow - s_lo));
+        const int gpr = group >> 7;  // 128-column groups per scale
+        int sidx = gb / gpr, ssub = gb - (gb / gpr) * gpr;
+        const int i = lane >> 3, w = lane & 7;
+        const float sv = i == 0 ? 0x1p69f : (i == 1 ? 0x1p67f : 0x1p65f);  // 2^(69 - p_i)
+        const __nv_bfloat162 f = __floats2bfloat162_rn(sv, sv);
+        const int boff = (2 * w + (i >> 1)) * TC_LBO + (i & 1) * 8;
+        for (int st = 0; st < nst + 2; st++) {
+            const int s = st % TC_NS;
+            if (st < nst && !mbar_wait(&full[s], (st / TC_NS) & 1)) {
                 failed = true;
                 break;
             }
-            if (gi >= TC_NA) {  // the buffer's previous group: its sums, then the buffer is free
-                if (!mbar_wait(&mdone[a], ((gi - TC_NA) / TC_NA) & 1)) {
+            // accumulators of stage st - 2: issue the loads, consume them after the B tiles
+            float dv[4][DW];
+            const int e0 = 4 * (st - 2), ne = st >= 2 ? (NGc - e0 < 4 ? NGc - e0 : 4) : 0;
+            if (ne > 0) {
+                if (st == 2 && !mbar_wait(sfull, 0)) {
+                    failed = true;
+                    break;
+                }
+                bool ok = true;
+                for (int u = 0; u < ne && ok; u++) ok = mbar_wait(&mdone[(e0 + u) % TC_ND], ((e0 + u) / TC_ND) & 1);
+                if (!ok) {
                     failed = true;
                     break;
                 }
                 tc_fence_after();
-                epilogue(gi - TC_NA);
+                // all four slots are loaded (a slot past the last group holds stale sums, unused)
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    const uint32_t dcol = tq + TC_DCOL + 16 * ((e0 + u) % TC_ND);
+                    if constexpr (DW == 8)
+                        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                                     : "=f"(dv[u][0]), "=f"(dv[u][1]), "=f"(dv[u][2]), "=f"(dv[u][3]),
+                                       "=f"(dv[u][4]), "=f"(dv[u][5]), "=f"(dv[u][6]), "=f"(dv[u][7])
+                                     : "r"(dcol)
+                                     : "memory");
+                    else
+                        asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                                     : "=f"(dv[u][0]), "=f"(dv[u][1]), "=f"(dv[u][2]), "=f"(dv[u][3])
+                                     : "r"(dcol)
+                                     : "memory");
+                }
             }
-            const uint8_t* stg = stages + s * TC_STAGE;
-            if (warp < m) {  // B tile row j = warp: x/s for the group's 128 columns, TMEM column order
-                const int col = 128 * gl + 4 * lane, b = col >> 8, c = col & 255;
-                const uint2 v = *reinterpret_cast<const uint2*>(stg + TC_CODES + ((b * m + warp) * 256 + c) * 2);
-                const int i = lane >> 3, w = lane & 7;
-                const float sv = i == 0 ? 128.f : (i == 1 ? 32.f : 8.f);  // 1/s of sub-block i
-                const __nv_bfloat162 f = __floats2bfloat162_rn(sv, sv);
-                const uint32_t lo = bf162_bits(__hmul2(bits_bf162(__byte_perm(v.x, v.y, 0x5410)), f));
-                const uint32_t hi = bf162_bits(__hmul2(bits_bf162(__byte_perm(v.x, v.y, 0x7632)), f));
-                *reinterpret_cast<uint2*>(btile + a * TC_BT + (2 * w + (i >> 1)) * 128 + warp * 16 + (i & 1) * 8) =
-                    make_uint2(lo, hi);
+            // B tiles of stage st (their slots are the accumulators just loaded): rows qd, qd + 4
+            const int g0 = 4 * st, nb = st < nst ? (NGc - g0 < 4 ? NGc - g0 : 4) : 0;
+            const uint8_t* xs = stages + s * TC_STAGE + TC_CODES;
+#pragma unroll
+            for (int jj = 0; jj < 2; jj++) {
+                const int j = qd + 4 * jj;
+                if (j >= m) break;
+#pragma unroll
+                for (int gl = 0; gl < 4; gl++) {
+                    if (gl < nb) {
+                        const int col = 128 * gl + 4 * lane;
+                        const uint2 v = *reinterpret_cast<const uint2*>(xs + (((col >> 8) * m + j) * 256 + (col & 255)) * 2);
+                        const uint32_t lo = bf162_bits(__hmul2(bits_bf162(__byte_perm(v.x, v.y, 0x5410)), f));
+                        const uint32_t hi = bf162_bits(__hmul2(bits_bf162(__byte_perm(v.x, v.y, 0x7632)), f));
+                        *reinterpret_cast<uint2*>(btile + ((g0 + gl) % TC_ND) * TC_BT + boff + j * 16) = make_uint2(lo, hi);
+                    }
+                }
             }
-            uint4 cw;
-            if (lane < TC_RQ)
-                cw = *reinterpret_cast<const uint4*>(stg + rho * 128 + (((2 * gl + hh) ^ (rho & 7)) << 4));
-            else
-                cw = make_uint4(0xAAAAAAAAu, 0xAAAAAAAAu, 0xAAAAAAAAu, 0xAAAAAAAAu);  // every code 2
-            uint32_t r[32];
-            unpack_group(cw, r);
-            tc_st32(tq + TC_ACOL + 64 * a + 32 * hh, r);
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            if (ne > 0) asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&afull[a]);
-                if (gl == 3 || gi == NGc - 1) mbar_arrive(&empty[s]);
+                for (int gl = 0; gl < nb; gl++) mbar_arrive(&bfull[(g0 + gl) % TC_ND]);
+                if (st < nst) mbar_arrive(&empty[s]);
+            }
+            // sums of stage st - 2: row minus the all-codes-2 row (lane 31), times the group scale
+            if (ne > 0) {
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    const bool live = u < ne;  // warp-uniform; no branch around the shuffles
+                    const float ds = rowok && live ? bf16_bits_to_f32(myscale[sidx]) : 0.f;
+                    if (live && ++ssub == gpr) {
+                        ssub = 0;
+                        sidx++;
+                    }
+#pragma unroll
+                    for (int j = 0; j < MV; j++) {
+                        const float off = __shfl_sync(0xffffffffu, dv[u][j], 31);
+                        const float t = fmaf(ds, dv[u][j] - off, tot[j]);
+                        tot[j] = live ? t : tot[j];
+                    }
+                }
             }
         }
-        if (!failed) {
-            for (int ge = NGc - TC_NA > 0 ? NGc - TC_NA : 0; ge < NGc; ge++) {
-                if (!mbar_wait(&mdone[ge % TC_NA], (ge / TC_NA) & 1)) {
+        tc_fence_before();
+    } else {  // unpack warps: two per lane quadrant, each half of a row's 32 code bytes, a pair of groups at a time
+        const int qd = warp & 3, hh = warp >> 2;
+        const int rho = TC_RQ * qd + lane;
+        const uint32_t tq = tbase + ((uint32_t)(32 * qd) << 16);
+        const int npr = (NGc + 1) >> 1;
+        for (int pr = 0; pr < npr; pr++) {
+            const int b = pr % TC_NAB, st = pr >> 1, s = st % TC_NS, g0 = 2 * pr;
+            if (!(pr & 1) && !mbar_wait(&full[s], (st / TC_NS) & 1)) {
+                failed = true;
+                break;
+            }
+            uint4 c0, c1;
+            if (lane < TC_RQ) {
+                const uint8_t* row = stages + s * TC_STAGE + rho * 128;
+                const int gl = g0 & 3;
+                c0 = *reinterpret_cast<const uint4*>(row + (((2 * gl + hh) ^ (rho & 7)) << 4));
+                c1 = *reinterpret_cast<const uint4*>(row + (((2 * gl + 2 + hh) ^ (rho & 7)) << 4));
+            } else {
+                c0 = c1 = make_uint4(0xAAAAAAAAu, 0xAAAAAAAAu, 0xAAAAAAAAu, 0xAAAAAAAAu);  // every code 2
+            }
+            uint32_t r0v[32], r1v[32];
+            unpack_group(c0, r0v);
+            unpack_group(c1, r1v);
+            if (pr >= TC_NAB) {  // A block b is free once the MMAs of pair pr - 3 are complete
+                const int gp = 2 * (pr - TC_NAB);
+                if (!mbar_wait(&mdone[gp % TC_ND], (gp / TC_ND) & 1) ||
+                    !mbar_wait(&mdone[(gp + 1) % TC_ND], ((gp + 1) / TC_ND) & 1)) {
                     failed = true;
                     break;
                 }
                 tc_fence_after();
-                epilogue(ge);
+            }
+            const uint32_t ta = tq + TC_ACOL + 128 * b + 32 * hh;
+            tc_st32(ta, r0v);
+            tc_st32(ta + 64, r1v);  // past the last group: an unused half of the block
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&afull[b]);
+                if ((pr & 1) || pr == npr - 1) mbar_arrive(&empty[s]);
             }
         }
         tc_fence_before();
@@ -339,35 +438,32 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (failed) atomicOr(&g_gemv_tc_status, 1u);
 
     // ------------------------------------------------------------------ partial sums -> y
-    const bool owner = warp < TC_UW && lane < TC_RQ && rho < R;
+    const int orow = TC_RQ * (warp & 3) + lane;
+    const bool owner = warp >= TC_EW0 && warp < TC_IW0 && lane < TC_RQ && orow < R;
     __syncwarp();
     if (csplit > 1) {
         if (owner) {
 #pragma unroll
-            for (int j = 0; j < 4; j++)
-                if (4 * hh + j < m) red[(4 * hh + j) * TC_ROWS + rho] = tot[j];
+            for (int j = 0; j < MV; j++) red[j * TC_ROWS + orow] = tot[j];
         }
         cluster_sync_all();
         if (rank == 0 && owner) {
             for (int q = 1; q < csplit; q++) {
 #pragma unroll
-                for (int j = 0; j < 4; j++)
-                    if (4 * hh + j < m) tot[j] += ld_cluster_f32(&red[(4 * hh + j) * TC_ROWS + rho], (uint32_t)q);
+                for (int j = 0; j < MV; j++) tot[j] += ld_cluster_f32(&red[j * TC_ROWS + orow], (uint32_t)q);
             }
         }
     }
     if (rank == 0 && owner) {
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-            if (4 * hh + j < m) {
-                const __nv_bfloat16 bv = __float2bfloat16_rn(tot[j]);
-                y[(size_t)(4 * hh + j) * n + r0 + rho] = *reinterpret_cast<const uint16_t*>(&bv);
-            }
+        for (int j = 0; j < MV; j++) {
+            const __nv_bfloat16 bv = __float2bfloat16_rn(tot[j] * 0x1p64f);
+            y[(size_t)j * n + r0 + orow] = *reinterpret_cast<const uint16_t*>(&bv);
         }
     }
     if (csplit > 1) cluster_sync_all();  // peers keep their shared memory until the leader has read it
     __syncthreads();
-    if (warp == TC_UW) {
+    if (warp == TC_IW0) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "n"(TC_TMEM_COLS));
     }
@@ -377,7 +473,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 int launch_q2_gemv_tc(const uint16_t* x, const bq_q2_weight* w, uint16_t* y, uint32_t m, cudaStream_t stream,
                       const char* who) {
     const int n = (int)w->n, k = (int)w->k, group = (int)w->group;
-    const int NG = k / 128;
+    const int NG = k / 128, G = k / group;
     const int nsm = sm_count();
     // clusters of `csplit` CTAs split K; every cluster owns <= 124 rows
     const int g0 = (n + TC_ROWS - 1) / TC_ROWS;
@@ -392,25 +488,36 @@ int launch_q2_gemv_tc(const uint16_t* x, const bq_q2_weight* w, uint16_t* y, uin
         if (nclus > n) nclus = n;
     }
     const int rows_hi = (n + nclus - 1) / nclus;
-    const int ngmax = (NG + csplit - 1) / csplit;
-    const size_t smem = 1024 + (size_t)TC_NS * TC_STAGE + TC_NA * TC_BT + 8 * TC_ROWS * 4 +
-                        (((size_t)ngmax * TC_ROWS + 7) & ~size_t(7)) * 2 + (2 * TC_NS + 2 * TC_NA) * 8 + 16;
+    const int sc_cap = (rows_hi * G * 2 + 32 + 15) & ~15;
+    const size_t smem = 1024 + (size_t)TC_NS * TC_STAGE + TC_ND * TC_BT + 8 * TC_ROWS * 4 + sc_cap + TC_NBAR * 8 + 16;
     if (smem > (size_t)TC_SMEM_LIMIT)
-        return fail(BQ_ERR_INVALID, "%s: k = %d needs %zu bytes of shared memory for its scales", who, k, smem);
+        return fail(BQ_ERR_INVALID, "%s: k/group = %d scales per row need %zu bytes of shared memory", who, G, smem);
 
-    static int configured[64] = {0};
+    static int configured[64][8] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 63;
-    if ((size_t)configured[dev] < smem) {
-        if (cudaFuncSetAttribute(q2_gemv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
+    void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, const uint8_t*, uint16_t*, int, int, int, int, int, int,
+                 int) = nullptr;
+    switch (m) {
+        case 1: kern = q2_gemv_tc_kernel<1>; break;
+        case 2: kern = q2_gemv_tc_kernel<2>; break;
+        case 3: kern = q2_gemv_tc_kernel<3>; break;
+        case 4: kern = q2_gemv_tc_kernel<4>; break;
+        case 5: kern = q2_gemv_tc_kernel<5>; break;
+        case 6: kern = q2_gemv_tc_kernel<6>; break;
+        case 7: kern = q2_gemv_tc_kernel<7>; break;
+        case 8: kern = q2_gemv_tc_kernel<8>; break;
+        default: return fail(BQ_ERR_INVALID, "%s: m = %u, must be 1..8", who, m);
+    }
+    if ((size_t)configured[dev][m - 1] < smem) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return fail(BQ_ERR_LAUNCH, "%s: cannot reserve %zu bytes of shared memory", who, smem);
-        configured[dev] = (int)smem;
+        configured[dev][m - 1] = (int)smem;
     }
 
     const uint8_t* codes = static_cast<const uint8_t*>(w->data);
-    const uint16_t* scales = reinterpret_cast<const uint16_t*>(codes + (size_t)n * (k / 4));
+    const uint8_t* splane = codes + (size_t)n * (k / 4);
     CUtensorMap cmap_hi, cmap_lo, xmap;
     int st = make_tmap_2d_u8(&cmap_hi, codes, k / 4, n, k / 4, 128, rows_hi, true, who);
     if (st) return st;
@@ -437,8 +544,8 @@ int launch_q2_gemv_tc(const uint16_t* x, const bq_q2_weight* w, uint16_t* y, uin
     }
     cfg.attrs = attrs;
     cfg.numAttrs = na;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, q2_gemv_tc_kernel, cmap_hi, cmap_lo, xmap, scales, y, (int)m, n, k,
-                                             group, nclus, csplit, rows_hi, ngmax);
+    const cudaError_t e =
+        cudaLaunchKernelEx(&cfg, kern, cmap_hi, cmap_lo, xmap, splane, y, n, k, group, nclus, csplit, rows_hi, sc_cap);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction ? BQ_ERR_UNSUPPORTED
