@@ -42,6 +42,7 @@ constexpr int GEMV_MAX_STAGES = 4;
 constexpr int GEMV_BOX = 16 * 128;                    // one codes box: 16 rows x 128 bytes
 constexpr int GEMV_XBOX = 256;                        // activations per x box row (bf16)
 constexpr int GEMV_SMEM_LIMIT = 225 * 1024;
+constexpr int GEMV_SMEM_SHARE = 112 * 1024;            // two CTAs per SM
 
 static __device__ unsigned int g_gemv_status;
 
@@ -120,15 +121,28 @@ struct GemvStage {
 // Requests chunk c into stage s: the codes of the CTA's rows (one box per 128-byte half;
 // `tmap` has a box of exactly nt*16 rows) and the chunk's activation columns.
 template <int T>
-__device__ __forceinline__ void gemv_issue(uint8_t* stages, int stage_bytes, uint64_t* full, const CUtensorMap* tmap,
-                                           const CUtensorMap* xmap, int c, int s, int nt, int r0, int m) {
+__device__ __forceinline__ void gemv_issue_codes(uint8_t* stages, int stage_bytes, uint64_t* full,
+                                                 const CUtensorMap* tmap, int c, int s, int nt, int r0, int m) {
     uint8_t* dst = stages + s * stage_bytes;
     mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * nt * GEMV_BOX + 4 * m * GEMV_XBOX * 2));
     tma_load_2d(dst, tmap, c * 256, r0, &full[s]);
     tma_load_2d(dst + T * GEMV_BOX, tmap, c * 256 + 128, r0, &full[s]);
+}
+
+template <int T>
+__device__ __forceinline__ void gemv_issue_x(uint8_t* stages, int stage_bytes, uint64_t* full, const CUtensorMap* xmap,
+                                             int c, int s, int m) {
+    uint8_t* dst = stages + s * stage_bytes;
     for (int j = 0; j < 4; j++)
         tma_load_2d(dst + GemvStage<T>::CODES + j * m * GEMV_XBOX * 2, xmap, c * (GEMV_PBLK * 128) + j * GEMV_XBOX, 0,
                     &full[s]);
+}
+
+template <int T>
+__device__ __forceinline__ void gemv_issue(uint8_t* stages, int stage_bytes, uint64_t* full, const CUtensorMap* tmap,
+                                           const CUtensorMap* xmap, int c, int s, int nt, int r0, int m) {
+    gemv_issue_codes<T>(stages, stage_bytes, full, tmap, c, s, nt, r0, m);
+    gemv_issue_x<T>(stages, stage_bytes, full, xmap, c, s, m);
 }
 
 template <int T>
@@ -141,10 +155,11 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1)
     uint8_t* stages = align1024(smem_raw);
     const int stage_bytes = (GemvStage<T>::bytes(m) + 1023) & ~1023;
     const int G = k / group;
-    // group scales as fp32 pairs (row r, row r + 8) per (tile, group, g)
-    float2* sc_s = reinterpret_cast<float2*>(stages + nstages * stage_bytes);
-    uint64_t* full = reinterpret_cast<uint64_t*>(sc_s + 8 * T * G);
-    uint32_t* released = reinterpret_cast<uint32_t*>(full + GEMV_MAX_STAGES);  // per stage: warps done with it
+    // the CTA's rows of the BF16 scale plane, from byte s_lo of the plane on
+    uint8_t* scs = stages + nstages * stage_bytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(scs + (((size_t)32 * T * G + 32 + 15) & ~size_t(15)));
+    uint64_t* sfull = full + GEMV_MAX_STAGES;                                   // scales landed
+    uint32_t* released = reinterpret_cast<uint32_t*>(sfull + 1);               // per stage: warps done with it
     int* issued = reinterpret_cast<int*>(released + GEMV_MAX_STAGES);          // per stage: last chunk requested
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -156,6 +171,15 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1)
     const int nch = (P + GEMV_PBLK - 1) / GEMV_PBLK;
     const int pre = nch < nstages ? nch : nstages;
     const CUtensorMap* tmap = nt == T ? &tmap_full : &tmap_less;
+    // scale bytes of rows r0 .. r0 + rows: [s_lo, s_hi) by one bulk copy, the rest (at most 14
+    // bytes at the end of the plane) by plain loads
+    const int rows = min(16 * nt, n - r0);
+    const uint8_t* splane = reinterpret_cast<const uint8_t*>(scales);
+    const int64_t s_lo = ((int64_t)r0 * G * 2) & ~int64_t(15), s_end = (int64_t)(r0 + rows) * G * 2;
+    int64_t s_hi = (s_end + 15) & ~int64_t(15);
+    const int64_t plane16 = ((int64_t)n * G * 2) & ~int64_t(15);
+    if (s_hi > plane16) s_hi = plane16;
+    if (s_hi < s_lo) s_hi = s_lo;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nstages; s++) {
@@ -163,29 +187,20 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1)
             released[s] = 0;
             issued[s] = s < pre ? s : -1;
         }
+        mbar_init(sfull, 1);
         fence_barrier_init();
-        for (int c = 0; c < pre; c++) gemv_issue<T>(stages, stage_bytes, full, tmap, &xmap, c, c, nt, r0, m);
+        // weights first: they do not depend on the kernel launched before this one
+        // (programmatic dependent launch); the activations once that kernel has finished
+        for (int c = 0; c < pre; c++) gemv_issue_codes<T>(stages, stage_bytes, full, tmap, c, c, nt, r0, m);
+        mbar_arrive_expect_tx(sfull, (uint32_t)(s_hi - s_lo));
+        if (s_hi > s_lo) bulk_load(scs, splane + s_lo, (uint32_t)(s_hi - s_lo), sfull);
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        for (int c = 0; c < pre; c++) gemv_issue_x<T>(stages, stage_bytes, full, &xmap, c, c, m);
     }
-    // this CTA's group scales, as (row 16tau + g, row 16tau + g + 8) fp32 pairs: element
-    // e = (8tau + gg)*G + gi runs along a row, so the loads coalesce; eight per thread in flight
-    for (int base = 0; base < 8 * T * G; base += 8 * GEMV_THREADS) {
-        uint16_t va[8], vb[8];
-#pragma unroll
-        for (int u = 0; u < 8; u++) {
-            const int e = base + u * GEMV_THREADS + threadIdx.x;
-            const int gi = e % G, pr = e / G, tau = pr >> 3;
-            const int ra = r0 + tau * 16 + (pr & 7), rb = ra + 8;
-            va[u] = e < 8 * T * G && tau < nt && ra < n ? __ldg(scales + (size_t)ra * G + gi) : (uint16_t)0;
-            vb[u] = e < 8 * T * G && tau < nt && rb < n ? __ldg(scales + (size_t)rb * G + gi) : (uint16_t)0;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; u++) {
-            const int e = base + u * GEMV_THREADS + threadIdx.x;
-            const int gi = e % G, pr = e / G;
-            if (e < 8 * T * G)
-                sc_s[((pr >> 3) * G + gi) * 8 + (pr & 7)] = make_float2(bf16_bits_to_f32(va[u]), bf16_bits_to_f32(vb[u]));
-        }
-    }
+    if (threadIdx.x == 32)  // scale bytes past the bulk copy
+        for (int64_t o = s_hi; o < s_end; o += 2)
+            *reinterpret_cast<uint16_t*>(scs + (o - s_lo)) = __ldg(reinterpret_cast<const uint16_t*>(splane + o));
     __syncthreads();
 
     bool failed = false;
@@ -249,13 +264,21 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1)
             gemv_step<5, TQ>(acc, wa, wb, b, mask, one);
             gemv_step<6, TQ>(acc, wa, wb, b, mask, one);
             gemv_step<7, TQ>(acc, wa, wb, b, mask, one);
+            if (c == 0 && !mbar_wait(sfull, 0)) {
+                failed = true;
+                break;
+            }
+            // scales of rows 16q + g and 16q + g + 8 (zero for tiles past nt)
+            const uint16_t* sr = reinterpret_cast<const uint16_t*>(scs + ((int64_t)(r0 + g) * G * 2 - s_lo)) + gi;
 #pragma unroll
             for (int q = 0; q < TQ; q++) {
-                const float2 d = sc_s[(q * G + gi) * 8 + g];
-                tot[q][0] = fmaf(d.x, acc[q][0], tot[q][0]);
-                tot[q][1] = fmaf(d.x, acc[q][1], tot[q][1]);
-                tot[q][2] = fmaf(d.y, acc[q][2], tot[q][2]);
-                tot[q][3] = fmaf(d.y, acc[q][3], tot[q][3]);
+                const bool v = q < nt;
+                const float da = v ? bf16_bits_to_f32(sr[(16 * q) * G]) : 0.f;
+                const float db = v ? bf16_bits_to_f32(sr[(16 * q + 8) * G]) : 0.f;
+                tot[q][0] = fmaf(da, acc[q][0], tot[q][0]);
+                tot[q][1] = fmaf(da, acc[q][1], tot[q][1]);
+                tot[q][2] = fmaf(db, acc[q][2], tot[q][2]);
+                tot[q][3] = fmaf(db, acc[q][3], tot[q][3]);
             }
         }
         // release the stage; the last warp to release it requests chunk c + nstages into it
@@ -316,9 +339,11 @@ static int launch_t(const uint8_t* codes, const CUtensorMap& xmap, const uint16_
     if (dev >= 64) dev = 63;
     const int G = k / group;
     const size_t stage = ((size_t)GemvStage<T>::bytes(m) + 1023) & ~size_t(1023);
-    const size_t fixed = 1024 + (size_t)8 * T * G * 8 + GEMV_MAX_STAGES * 16;
+    const size_t fixed = 1024 + (((size_t)32 * T * G + 32 + 15) & ~size_t(15)) + (GEMV_MAX_STAGES * 2 + 1) * 8 + 16;
+    // At most ~112 KB where two stages allow it, so the CTA of the next launch (programmatic
+    // dependent launch) can share the SM and start its weight copies before this one ends.
     int nstages = GEMV_MAX_STAGES;
-    while (nstages > 2 && fixed + nstages * stage > (size_t)GEMV_SMEM_LIMIT) nstages--;
+    while (nstages > 2 && fixed + nstages * stage > (size_t)GEMV_SMEM_SHARE) nstages--;
     const size_t smem = fixed + nstages * stage;
     if (smem > (size_t)GEMV_SMEM_LIMIT) return fail(BQ_ERR_INVALID, "%s: shape needs too much shared memory", who);
     if ((size_t)configured_smem[dev] < smem) {
@@ -332,9 +357,57 @@ static int launch_t(const uint8_t* codes, const CUtensorMap& xmap, const uint16_
     int st = make_tmap_2d_u8(&map_full, codes, k / 4, n, k / 4, 128, 16 * T, true, who);
     if (st) return st;
     if ((st = make_tmap_2d_u8(&map_less, codes, k / 4, n, k / 4, 128, T > 1 ? 16 * (T - 1) : 16, true, who))) return st;
-    q2_gemv_kernel<T><<<ncta, GEMV_THREADS, smem, stream>>>(map_full, map_less, xmap, scales, y, m, n, k, group,
-                                                            ntiles, nstages);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ncta);
+    cfg.blockDim = dim3(GEMV_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, q2_gemv_kernel<T>, map_full, map_less, xmap, scales, y, m, n, k, group, ntiles,
+                           nstages) != cudaSuccess)
+        return check_launch(who);
     return BQ_OK;
+}
+
+// The warp-MMA GEMV: CTA c takes a contiguous range of T or T - 1 row tiles.
+static int launch_q2_gemv_mma(const uint16_t* x, const bq_q2_weight* w, uint16_t* y, uint32_t m,
+                              cudaStream_t stream, const char* who) {
+    const int G = (int)(w->k / w->group);
+    const int ntiles = (int)((w->n + 15) / 16);
+    int tmax = GEMV_MAX_T;
+    while (tmax > 1 && (size_t)32 * tmax * G > 96 * 1024) tmax--;
+    if ((size_t)32 * tmax * G > 96 * 1024)
+        return fail(BQ_ERR_INVALID, "%s: k/group = %d groups per row is too many", who, G);
+    int ncta = ntiles < sm_count() ? ntiles : sm_count();
+    int T = (ntiles + ncta - 1) / ncta;
+    if (T > tmax) {
+        ncta = (ntiles + tmax - 1) / tmax;
+        T = (ntiles + ncta - 1) / ncta;  // every CTA then gets T or T - 1 tiles
+    }
+    const uint8_t* codes = (const uint8_t*)w->data;
+    const uint16_t* scales = (const uint16_t*)(codes + (size_t)w->n * (w->k / 4));
+    CUtensorMap xmap;
+    // activations x [m][k] as 16-bit elements, boxes of 256 columns x m rows
+    int st = make_tmap_2d(&xmap, x, 2, w->k, m, (uint64_t)w->k * 2, GEMV_XBOX, m, false, who);
+    if (st) return st;
+    const int mm = (int)m, n = (int)w->n, k = (int)w->k, gr = (int)w->group;
+    switch (T) {
+        case 1: st = launch_t<1>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
+        case 2: st = launch_t<2>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
+        case 3: st = launch_t<3>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
+        case 4: st = launch_t<4>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
+        case 5: st = launch_t<5>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
+        case 6: st = launch_t<6>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
+        case 7: st = launch_t<7>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
+        case 8: st = launch_t<8>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
+        default: return fail(BQ_ERR_INVALID, "%s: internal tile count %d", who, T);
+    }
+    if (st) return st;
+    return check_launch(who);
 }
 
 // Launches the GEMV for an already validated weight.
@@ -346,7 +419,7 @@ int launch_q2_gemv(const uint16_t* x, const bq_q2_weight* w, uint16_t* y, uint32
             return fail(BQ_ERR_LAUNCH, "%s: memset failed", who);
         return ok();
     }
-    return launch_q2_gemv_tc(x, w, y, m, stream, who);
+    return launch_q2_gemv_mma(x, w, y, m, stream, who);
 }
 
 static int check_gemv_args(const uint16_t* x, const bq_q2_weight* w, const uint16_t* y, uint32_t m, const char* who) {
