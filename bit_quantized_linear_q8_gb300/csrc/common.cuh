@@ -40,12 +40,7 @@ int make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t ro
 // Reads and clears each translation unit's device status word (nonzero after a bounded
 // wait gave up).
 unsigned int gemv_status_take();
-unsigned int gemv_tc_status_take();
 unsigned int mmq_status_take();
-
-// Launches the tcgen05 decode GEMV (gemv_tc.cu) for a validated weight, k > 0, n > 0, 1 <= m <= 8.
-int launch_q2_gemv_tc(const uint16_t* x, const bq_q2_weight* w, uint16_t* y, uint32_t m, cudaStream_t stream,
-                      const char* who);
 
 // ------------------------------------------------------------------ device helpers
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
