@@ -97,7 +97,7 @@ int make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t ro
 extern "C" {
 
 int bq_device_status(void) {
-    const unsigned int s = bq8::gemv_status_take() | bq8::mmq_status_take();
+    const unsigned int s = bq8::gemv_status_take() | bq8::mmq_status_take() | bq8::mmq_tc_status_take();
     if (s) return bq8::fail(BQ_ERR_DEVICE, "a kernel gave up on a bounded wait (status bits 0x%x)", s);
     return bq8::ok();
 }

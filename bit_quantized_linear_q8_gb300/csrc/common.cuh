@@ -41,6 +41,7 @@ int make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t ro
 // wait gave up).
 unsigned int gemv_status_take();
 unsigned int mmq_status_take();
+unsigned int mmq_tc_status_take();
 
 // ------------------------------------------------------------------ device helpers
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }

@@ -1,24 +1,23 @@
-// mmq.cu -- integer MMQ GEMMs: q8_1 activations x Q2_0 / block_q4_K weights, BF16 store.
+// mmq.cu -- Q4_K MMQ GEMM: q8_1 activations x block_q4_K weights, BF16 store.
 //
-// Sources: init_q2.rs `qkvz_q2_prefill_gemm` (MMQ route, group 128) and q4k_mmq.rs
-// `q4k_mmq_gemm` (C[m, n] = A[m, k] x W[n, k], 128 x 128 tiles, BF16 store).
+// Source: q4k_mmq.rs `q4k_mmq_gemm` (C[m, n] = A[m, k] x W[n, k], 128 x 128 tiles, BF16
+// store).  (The Q2_0 MMQ is in mmq_tc.cu.)
 //
 // Design (GB300, sm_103a).  The tcgen05 tensor cores of sm_103a have no int8 kind, and
-// q8_1's per-32 activation scale has to be applied to every 32-wide partial product, so the
-// contraction runs on the warp-level integer MMA (mma.sync m16n8k32, s8 x u8 -> s32), one
-// instruction per 32-value block, which gives the exact integer partial P_b of each block:
+// q8_1's per-32 activation scale and Q4_K's per-32 sub-block scale have to be applied to
+// every 32-wide partial product, so the contraction runs on the warp-level integer MMA
+// (mma.sync m16n8k32, s8 x u8 -> s32), one instruction per 32-value block, which gives the
+// exact integer partial P_j of each block:
 //
-//  * Staging: a producer warp streams, per 128-column K step, the CTA's q8_1 code tile
-//    (128 rows x 128 bytes, 128-byte swizzle), its (d, s) pairs and the weight tile through
-//    a 4-stage TMA / mbarrier ring.  Bounded waits throughout.
+//  * Staging: a producer warp streams, per 256-column K step (one super-block), the CTA's
+//    q8_1 code tile (128-byte swizzle), its (d, s) pairs and the weight blocks through a
+//    3-stage TMA / mbarrier ring.  Bounded waits throughout.
 //  * Compute: eight consumer warps, each a 64 (m) x 32 (n) warp tile = 4 x 4 MMAs per
 //    block.  A fragments come from ldmatrix on the swizzled tile; B fragments are built in
-//    registers straight from the packed codes (Q2_0: one shift + AND per 4 codes, because
-//    byte l of a pack block holds column 32i + l of each sub-block i).
+//    registers from the 4-bit codes.
 //  * Exact conversion: each MMA starts from the int32 bit pattern of 1.5 * 2^23, so its
-//    result reinterpreted as fp32 is exactly 1.5*2^23 + P_b; one packed fp32 add removes
-//    the offset, one packed FMA applies the activation scale d_a.  Per 128-column group
-//    the Q2 scale d_w and the code offset (-2 * sum of s) are applied.
+//    result reinterpreted as fp32 is exactly 1.5*2^23 + P_j; one packed fp32 add removes
+//    the offset, one packed FMA applies the scales.
 #include "common.cuh"
 
 namespace bq8 {
@@ -37,10 +36,6 @@ constexpr int MMQ_CWARPS = 8;
 constexpr int MMQ_THREADS = (MMQ_CWARPS + 1) * 32;
 constexpr int MMQ_STAGES = 4;
 constexpr int MMQ_TILE = 128;                  // BM = BN = 128, K step 128
-constexpr int Q2S_A = 0;                       // q8_1 codes, 128 x 128 B, swizzled
-constexpr int Q2S_D = 16384;                   // (d, s) pairs, 128 x 32 B
-constexpr int Q2S_B = 20480;                   // Q2 codes, 128 x 32 B
-constexpr int Q2S_STAGE = 24576;
 constexpr int MAGIC_I = 0x4B400000;            // bits of 1.5 * 2^23
 constexpr float MAGIC_F = 12582912.0f;
 
@@ -85,143 +80,6 @@ __device__ __forceinline__ void store_tile(const float2 (&acc)[4][4][2], uint16_
             }
         }
     }
-}
-
-__global__ void __launch_bounds__(MMQ_THREADS, 1)
-    q2_mmq_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapD,
-                  const __grid_constant__ CUtensorMap mapB, const uint16_t* __restrict__ wscales,
-                  uint16_t* __restrict__ out, int m, int n, int k) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* stages = align1024(smem_raw);
-    const int G = k >> 7;
-    uint16_t* sc_s = reinterpret_cast<uint16_t*>(stages + MMQ_STAGES * Q2S_STAGE);
-    uint64_t* bars =
-        reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(sc_s + MMQ_TILE * G) + 7) & ~uintptr_t(7));
-    uint64_t* full = bars;
-    uint64_t* empty = bars + MMQ_STAGES;
-
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int g = lane >> 2, t = lane & 3;
-    const int n0 = blockIdx.x * MMQ_TILE, m0 = blockIdx.y * MMQ_TILE;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < MMQ_STAGES; s++) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], MMQ_CWARPS);
-        }
-        fence_barrier_init();
-    }
-    {   // the weight tile's group scales (contiguous rows of the scale plane)
-        const int rows = min(MMQ_TILE, n - n0);
-        copy_to_smem(sc_s, wscales + (size_t)n0 * G, rows * G * 2, threadIdx.x, blockDim.x);
-        for (int idx = rows * G + threadIdx.x; idx < MMQ_TILE * G; idx += blockDim.x) sc_s[idx] = 0;
-    }
-    __syncthreads();
-
-    bool failed = false;
-    float2 acc[4][4][2];
-#pragma unroll
-    for (int a = 0; a < 4; a++)
-#pragma unroll
-        for (int b = 0; b < 4; b++) acc[a][b][0] = acc[a][b][1] = make_float2(0.f, 0.f);
-    const int wm = warp & 1, wn = warp >> 1;
-
-    if (warp == MMQ_CWARPS) {
-        if (lane == 0) {
-            for (int c = 0; c < G; c++) {
-                const int s = c % MMQ_STAGES;
-                if (c >= MMQ_STAGES && !mbar_wait(&empty[s], ((c / MMQ_STAGES) - 1) & 1)) {
-                    failed = true;
-                    break;
-                }
-                uint8_t* dst = stages + s * Q2S_STAGE;
-                mbar_arrive_expect_tx(&full[s], Q2S_STAGE);
-                tma_load_2d(dst + Q2S_A, &mapA, c * 128, m0, &full[s]);
-                tma_load_2d(dst + Q2S_D, &mapD, c * 32, m0, &full[s]);
-                tma_load_2d(dst + Q2S_B, &mapB, c * 32, n0, &full[s]);
-            }
-            const int first = G > MMQ_STAGES ? G - MMQ_STAGES : 0;
-            for (int c = first; c < G && !failed; c++)
-                if (!mbar_wait(&full[c % MMQ_STAGES], (c / MMQ_STAGES) & 1)) failed = true;
-        }
-    } else {
-        const int cmagic[4] = {MAGIC_I, MAGIC_I, MAGIC_I, MAGIC_I};
-        for (int c = 0; c < G; c++) {
-            const int s = c % MMQ_STAGES;
-            if (!mbar_wait(&full[s], (c / MMQ_STAGES) & 1)) {
-                failed = true;
-                break;
-            }
-            const uint8_t* A = stages + s * Q2S_STAGE + Q2S_A;
-            const uint8_t* D = stages + s * Q2S_STAGE + Q2S_D;
-            const uint8_t* Bt = stages + s * Q2S_STAGE + Q2S_B;
-            uint32_t w0[4], w1[4];
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-                const int row = wn * 32 + j * 8 + g;
-                w0[j] = *reinterpret_cast<const uint32_t*>(Bt + row * 32 + 4 * t);
-                w1[j] = *reinterpret_cast<const uint32_t*>(Bt + row * 32 + 16 + 4 * t);
-            }
-            float2 ag[4][4][2];
-#pragma unroll
-            for (int a = 0; a < 4; a++)
-#pragma unroll
-                for (int b = 0; b < 4; b++) ag[a][b][0] = ag[a][b][1] = make_float2(0.f, 0.f);
-            float ssum[4][2];
-#pragma unroll
-            for (int a = 0; a < 4; a++) ssum[a][0] = ssum[a][1] = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                float da[4][2];
-                uint32_t af[4][4];
-#pragma unroll
-                for (int mt = 0; mt < 4; mt++) {
-                    const int rlo = wm * 64 + mt * 16 + g;
-                    const float2 vlo = *reinterpret_cast<const float2*>(D + rlo * 32 + 8 * i);
-                    const float2 vhi = *reinterpret_cast<const float2*>(D + (rlo + 8) * 32 + 8 * i);
-                    da[mt][0] = vlo.x;
-                    da[mt][1] = vhi.x;
-                    ssum[mt][0] += vlo.y;
-                    ssum[mt][1] += vhi.y;
-                    const int rl = wm * 64 + mt * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
-                    const int ch = 2 * i + (lane >> 4);
-                    ldmatrix_x4(af[mt], A + rl * 128 + ((ch ^ (rl & 7)) << 4));
-                }
-#pragma unroll
-                for (int nt = 0; nt < 4; nt++) {
-                    const uint32_t b0 = (w0[nt] >> (2 * i)) & 0x03030303u;
-                    const uint32_t b1 = (w1[nt] >> (2 * i)) & 0x03030303u;
-#pragma unroll
-                    for (int mt = 0; mt < 4; mt++) {
-                        int d[4];
-                        mma_s8u8_16832(d, af[mt][0], af[mt][1], af[mt][2], af[mt][3], b0, b1, cmagic);
-                        ag[mt][nt][0] = __ffma2_rn(i2f_magic(d[0], d[1]), make_float2(da[mt][0], da[mt][0]),
-                                                   ag[mt][nt][0]);
-                        ag[mt][nt][1] = __ffma2_rn(i2f_magic(d[2], d[3]), make_float2(da[mt][1], da[mt][1]),
-                                                   ag[mt][nt][1]);
-                    }
-                }
-            }
-            // group epilogue: out += d_w * (sum_b d_a P_b - 2 sum_b s_b)
-#pragma unroll
-            for (int nt = 0; nt < 4; nt++) {
-                const int col = wn * 32 + nt * 8 + 2 * t;
-                const float2 dw = make_float2(bf16_bits_to_f32(sc_s[col * G + c]), bf16_bits_to_f32(sc_s[(col + 1) * G + c]));
-#pragma unroll
-                for (int mt = 0; mt < 4; mt++) {
-                    const float2 o0 = make_float2(-2.f * ssum[mt][0], -2.f * ssum[mt][0]);
-                    const float2 o1 = make_float2(-2.f * ssum[mt][1], -2.f * ssum[mt][1]);
-                    acc[mt][nt][0] = __ffma2_rn(__fadd2_rn(ag[mt][nt][0], o0), dw, acc[mt][nt][0]);
-                    acc[mt][nt][1] = __ffma2_rn(__fadd2_rn(ag[mt][nt][1], o1), dw, acc[mt][nt][1]);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-        }
-    }
-    if (failed) atomicOr(&g_mmq_status, 2u);
-
-    if (warp < MMQ_CWARPS) store_tile(acc, out, m, n, m0 + wm * 64, n0 + wn * 32, g, t);
 }
 
 // ------------------------------------------------------------------------------------
@@ -399,40 +257,6 @@ static int reserve_smem(const void* fn, size_t bytes, int* cache, const char* wh
 using namespace bq8;
 
 extern "C" {
-
-int q2_mmq_gemm(const void* act_q8, const bq_q2_weight* w, uint16_t* out, uint32_t m, bq_stream_t stream) {
-    const char* who = "q2_mmq_gemm";
-    int st = check_q2(w, who);
-    if (st) return st;
-    if (w->group != 128) return fail(BQ_ERR_INVALID, "%s: the MMQ route needs group size 128 (got %u)", who, w->group);
-    if (m == 0 || w->n == 0) return ok();
-    if (!out || !aligned16(out)) return fail(BQ_ERR_INVALID, "%s: out NULL or not 16-byte aligned", who);
-    if (w->k == 0) {
-        if (cudaMemsetAsync(out, 0, (size_t)m * w->n * 2, (cudaStream_t)stream) != cudaSuccess)
-            return fail(BQ_ERR_LAUNCH, "%s: memset failed", who);
-        return ok();
-    }
-    if (!act_q8 || !aligned16(act_q8)) return fail(BQ_ERR_INVALID, "%s: act_q8 NULL or not 16-byte aligned", who);
-    if (m > (1u << 24) || w->n > (1u << 24)) return fail(BQ_ERR_INVALID, "%s: shape too large", who);
-    const uint64_t kp = ((uint64_t)w->k + 255) / 256 * 256;
-    const uint8_t* codes = (const uint8_t*)act_q8;
-    const uint8_t* ds = codes + (uint64_t)m * kp;
-    const uint8_t* wcodes = (const uint8_t*)w->data;
-    const uint16_t* wsc = (const uint16_t*)(wcodes + (size_t)w->n * (w->k / 4));
-    CUtensorMap mA, mD, mB;
-    if ((st = make_tmap_2d_u8(&mA, codes, kp, m, kp, 128, 128, true, who))) return st;
-    if ((st = make_tmap_2d_u8(&mD, ds, kp / 4, m, kp / 4, 32, 128, false, who))) return st;
-    if ((st = make_tmap_2d_u8(&mB, wcodes, w->k / 4, w->n, w->k / 4, 32, 128, false, who))) return st;
-    const int G = (int)(w->k / 128);
-    const size_t smem = 1024 + (size_t)MMQ_STAGES * Q2S_STAGE + (size_t)MMQ_TILE * G * 2 + 8 + 2 * MMQ_STAGES * 8;
-    if (smem > 227 * 1024) return fail(BQ_ERR_INVALID, "%s: k = %u too large for the scale buffer", who, w->k);
-    static int cache[64] = {0};
-    if ((st = reserve_smem((const void*)q2_mmq_kernel, smem, cache, who))) return st;
-    const dim3 grid((w->n + MMQ_TILE - 1) / MMQ_TILE, (m + MMQ_TILE - 1) / MMQ_TILE);
-    q2_mmq_kernel<<<grid, MMQ_THREADS, smem, (cudaStream_t)stream>>>(mA, mD, mB, wsc, out, (int)m, (int)w->n,
-                                                                      (int)w->k);
-    return check_launch(who);
-}
 
 int q4k_mmq_gemm(const void* act_q8, const void* w_q4k, uint16_t* out, uint32_t m, uint32_t n, uint32_t k,
                  bq_stream_t stream) {

@@ -1,0 +1,410 @@
+// mmq_tc.cu -- Q2_0 MMQ on the tcgen05 tensor cores: q8_1 activations x Q2_0 weights, BF16 store.
+//
+// Source: init_q2.rs `qkvz_q2_prefill_gemm` (MMQ route, group 128):
+//     out[m, n] = sum_k (d_a q)[m, k] * (d_w (c - 2))[n, k]
+// with q8_1 activation values d_a * q (one fp32 d_a per 32 values) and Q2_0 weights
+// d_w * (c - 2) (one BF16 d_w per 128 values).
+//
+// Design (GB300, sm_103a).  The tcgen05 tensor cores of sm_103a have no int8 kind, so the
+// contraction runs on the BF16 kind (kind::f16, fp32 accumulation in tensor memory) with
+// operands that carry the quantised values:
+//  * Weights: d_w * (c - 2) is exact in BF16 (a BF16 scale times -2, -1, 0 or 1), so the group
+//    scale and the code offset are part of the operand and nothing per group is left over.
+//  * Activations: v = d_a * q (fp32) is split into hi = bf16(v) and lo = bf16(v - hi); hi + lo
+//    equals v to 2^-17 relative.  Each K step multiplies both halves with the same weight
+//    operand into the same accumulator (two MMAs per K16), so the per-32 activation scale is
+//    inside the operand too and the accumulator is read only once, at the end.
+//  Every product of two BF16 values is exact in fp32; the sums are the tensor cores' fp32.
+//
+//  * Tile 128 (m) x 256 (n), K step 64.  Tensor memory holds the accumulator (256 columns)
+//    and four stages of the activation operand (A from tensor memory: lane = row, column j =
+//    K elements 2j, 2j+1; 32 columns hi + 32 columns lo per stage).  Shared memory holds four
+//    stages of the weight operand (256 x 64 BF16, no-swizzle K-major 8 x 16-byte core
+//    matrices).  No global scratch.
+//  * Warp 0 allocates tensor memory; one lane issues M128 N256 K16 MMAs (8 per K step) and
+//    commits each step to the stage's `empty` barrier.
+//  * Warps 1-4 (one per tensor-memory lane quadrant, one activation row per thread) expand
+//    the q8_1 codes into the hi/lo operand with tcgen05.st, then run the epilogue
+//    (tcgen05.ld -> BF16 -> global).
+//  * Warps 5-12 (one weight row per thread) expand the 2-bit codes into shared memory.
+//  * K order inside a step: the 64 columns of step s are those of pack block s/2 with
+//    in-block offsets 32i + 16(s%2) + l (i = 0..3, l = 0..15), and 32-bit operand word
+//    q = 8u + 2i + j holds offsets (l = 4u + j, l = 4u + j + 2).  In the Q2 layout (byte l of a
+//    pack block holds the codes of offsets 32i + l in bits 2i) those two codes sit 16 bits
+//    apart in one 32-bit word of packed codes, so one shift and one LOP3 place a pair of codes
+//    into a BF16 pair.  Both operands use this order, so the contraction is unchanged.
+//  * Every wait is bounded; a wait that gives up raises the CTA's abort flag and the status
+//    word, and the kernel winds down (it still waits for its own MMAs before freeing tensor
+//    memory).
+#include "common.cuh"
+
+namespace bq8 {
+
+static __device__ unsigned int g_mmq_tc_status;
+
+unsigned int mmq_tc_status_take() {
+    unsigned int v = 0, zero = 0;
+    cudaDeviceSynchronize();
+    cudaMemcpyFromSymbol(&v, g_mmq_tc_status, sizeof v);
+    cudaMemcpyToSymbol(g_mmq_tc_status, &zero, sizeof zero);
+    return v;
+}
+
+constexpr int QT_BM = 128;
+constexpr int QT_BN = 256;
+constexpr int QT_NS = 4;                         // K-step stages (tensor memory and shared memory)
+constexpr int QT_AWARP0 = 1;                     // warps 1..4: activation operand, epilogue
+constexpr int QT_BWARP0 = 5;                     // warps 5..12: weight operand
+constexpr int QT_THREADS = 13 * 32;
+constexpr uint32_t QT_BSTAGE = QT_BN * 64 * 2;   // 32 KB of weight operand per stage
+constexpr uint32_t QT_TMEM_COLS = 512;
+constexpr uint32_t QT_ACOL = 256;                // first column of the activation stages
+constexpr uint32_t QT_WAIT_LIMIT = 1u << 22;     // polls (~64 ns each) before a wait gives up
+static_assert(QT_ACOL + 64 * QT_NS <= QT_TMEM_COLS, "tensor memory budget");
+static_assert(QT_BWARP0 == QT_AWARP0 + 4 && QT_THREADS == (QT_BWARP0 + QT_BN / 32) * 32, "warp roles");
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bit 4), A and B BF16 (bits 7-9,
+// 10-12), both K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t QT_IDESC =
+    (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(QT_BN >> 3) << 17) | ((uint32_t)(QT_BM >> 4) << 24);
+
+// Shared-memory matrix descriptor, no swizzle: 8-row x 16-byte core matrices, `lbo` bytes
+// apart along K, `sbo` bytes apart along N; bit 46 is the descriptor version.
+__device__ __forceinline__ uint64_t qt_smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, M128 N256 K16, BF16 in, fp32 accumulate.
+__device__ __forceinline__ void qt_mma(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.u32 p, %3, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n}\n" ::"r"(d),
+        "r"(a), "l"(bdesc), "r"(accumulate), "r"(QT_IDESC));
+}
+
+__device__ __forceinline__ void qt_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void qt_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void qt_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void qt_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void qt_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Bounded wait that also gives up as soon as another thread of the CTA has raised `abort`.
+__device__ __forceinline__ bool qt_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    for (uint32_t it = 0; it < QT_WAIT_LIMIT; it++) {
+        if (mbar_test(bar, parity)) return true;
+        if (*abort) return false;
+        __nanosleep(32);
+    }
+    *abort = 1;
+    atomicOr(&g_mmq_tc_status, 1u);
+    return false;
+}
+
+// The same for a whole warp, with a warp-uniform answer (the callers go on to .sync.aligned
+// tensor-memory instructions).
+__device__ __forceinline__ bool qt_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    const bool ok = qt_wait(bar, parity, abort);
+    return __all_sync(0xffffffffu, ok) != 0;
+}
+
+// Two signed int8 codes (bytes b0 and b1 of `w`, biased by 0x80) times d, as fp32, split into
+// a BF16 pair hi and a BF16 pair lo with hi + lo = d * q to 2^-17.
+__device__ __forceinline__ void qt_split_pair(uint32_t wb, uint32_t sel0, uint32_t sel1, float d, uint32_t& hi,
+                                              uint32_t& lo) {
+    // 0x4B0000xx is the float 2^23 + xx; subtracting 2^23 + 128 leaves the signed code exactly.
+    const float f0 = __uint_as_float(__byte_perm(wb, 0x4B000000u, sel0));
+    const float f1 = __uint_as_float(__byte_perm(wb, 0x4B000000u, sel1));
+    const float2 v = __fmul2_rn(__fadd2_rn(make_float2(f0, f1), make_float2(-8388736.0f, -8388736.0f)),
+                                make_float2(d, d));
+    hi = bf162_bits(__floats2bfloat162_rn(v.x, v.y));
+    const float2 h = make_float2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xFFFF0000u));
+    const float2 r = __fadd2_rn(v, make_float2(-h.x, -h.y));
+    lo = bf162_bits(__floats2bfloat162_rn(r.x, r.y));
+}
+
+__device__ __forceinline__ uint32_t u4_get(const uint4& v, int u) {
+    return u == 0 ? v.x : u == 1 ? v.y : u == 2 ? v.z : v.w;
+}
+
+__global__ void __launch_bounds__(QT_THREADS, 1)
+    q2_mmq_tc_kernel(const uint8_t* __restrict__ acodes, const float* __restrict__ ads, int kp,
+                     const uint8_t* __restrict__ wcodes, const uint16_t* __restrict__ wsc,
+                     uint16_t* __restrict__ out, int m, int n, int k, int ntn) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* bst = align1024(smem_raw);
+    uint64_t* afull = reinterpret_cast<uint64_t*>(bst + QT_NS * QT_BSTAGE);
+    uint64_t* bfull = afull + QT_NS;
+    uint64_t* sempty = bfull + QT_NS;
+    uint64_t* accfull = sempty + QT_NS;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(accfull + 1);
+    volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int n0 = (blockIdx.x % ntn) * QT_BN, m0 = (blockIdx.x / ntn) * QT_BM;
+    const int S = k >> 6;  // K steps of 64
+    const int G = k >> 7;  // groups of 128 (one BF16 scale each)
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < QT_NS; s++) {
+            mbar_init(&afull[s], 4 * 32);
+            mbar_init(&bfull[s], 8 * 32);
+            mbar_init(&sempty[s], 1);
+        }
+        mbar_init(accfull, 1);
+        *abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                     "n"(QT_TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    qt_fence_before();
+    __syncthreads();
+    qt_fence_after();
+    const uint32_t tbase = *tslot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int s = 0; s < S; s++) {
+                const int st = s % QT_NS;
+                const uint32_t par = (uint32_t)(s / QT_NS) & 1u;
+                if (!qt_wait(&afull[st], par, abort) || !qt_wait(&bfull[st], par, abort)) break;
+                qt_fence_after();
+                const uint32_t bbase = smem_u32(bst + st * QT_BSTAGE);
+                const uint32_t abase = tbase + QT_ACOL + 64u * st;
+#pragma unroll
+                for (int kk = 0; kk < 4; kk++) {
+                    const uint64_t bd = qt_smem_desc(bbase + 256u * kk, 128u, 1024u);
+                    qt_mma(tbase, abase + 8u * kk, bd, (s | kk) != 0);
+                    qt_mma(tbase, abase + 32u + 8u * kk, bd, 1u);
+                }
+                qt_commit(&sempty[st]);
+            }
+            qt_commit(accfull);  // completes once every MMA issued above has finished
+            if (!mbar_wait(accfull, 0)) atomicOr(&g_mmq_tc_status, 2u);
+        }
+        __syncwarp();
+    } else if (warp < QT_BWARP0) {
+        // ---------------------------------------------------------------- activation operand
+        const int qd = warp & 3;  // tensor-memory lane quadrant this warp may access
+        const uint32_t tA = tbase + ((uint32_t)(32 * qd) << 16);
+        const int row = m0 + 32 * qd + lane;
+        const bool rv = row < m;
+        const uint8_t* arow = acodes + (size_t)(rv ? row : 0) * kp;
+        const float* drow = ads + (size_t)(rv ? row : 0) * (kp / 16);
+        uint4 cr[4], nr[4];
+        float cd[4], nd[4];
+        auto load = [&](int s, uint4 (&r)[4], float (&dd)[4]) {
+            const int pb = s >> 1, h = s & 1;
+            if (rv) {
+#pragma unroll
+                for (int i = 0; i < 4; i++) r[i] = ldg_nc128(arow + 128 * pb + 32 * i + 16 * h);
+                const uint4 p0 = ldg_nc128(drow + 8 * pb);
+                const uint4 p1 = ldg_nc128(drow + 8 * pb + 4);
+                dd[0] = __uint_as_float(p0.x);
+                dd[1] = __uint_as_float(p0.z);
+                dd[2] = __uint_as_float(p1.x);
+                dd[3] = __uint_as_float(p1.z);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    r[i] = make_uint4(0u, 0u, 0u, 0u);  // code 0 (after the 0x80 bias below), d = 0
+                    dd[i] = 0.f;
+                }
+            }
+        };
+        load(0, cr, cd);
+        for (int s = 0; s < S; s++) {
+            const int st = s % QT_NS;
+            if (s + 1 < S) load(s + 1, nr, nd);
+            if (s >= QT_NS) {
+                if (!qt_wait_warp(&sempty[st], (uint32_t)((s / QT_NS) - 1) & 1u, abort)) break;
+                qt_fence_after();
+            }
+            const uint32_t tcol = tA + QT_ACOL + 64u * st;
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                uint32_t hw[8], lw[8];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const uint32_t wb = u4_get(cr[i], u) ^ 0x80808080u;
+                    // word 8u + 2i + j: offsets 4u + j (low half) and 4u + j + 2 (high half)
+                    qt_split_pair(wb, 0x7540u, 0x7542u, cd[i], hw[2 * i], lw[2 * i]);
+                    qt_split_pair(wb, 0x7541u, 0x7543u, cd[i], hw[2 * i + 1], lw[2 * i + 1]);
+                }
+                qt_st8(tcol + 8u * u, hw);
+                qt_st8(tcol + 32u + 8u * u, lw);
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            qt_fence_before();
+            mbar_arrive(&afull[st]);
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                cr[i] = nr[i];
+                cd[i] = nd[i];
+            }
+        }
+        // ---------------------------------------------------------------- epilogue
+        bool ok = mbar_wait(accfull, 0);
+        ok = __all_sync(0xffffffffu, ok && !*abort) != 0;
+        qt_fence_after();
+        if (ok) {
+            const bool vec = (n & 7) == 0;
+#pragma unroll 1
+            for (int c = 0; c < QT_BN / 32; c++) {
+                const int col0 = n0 + 32 * c;
+                if (col0 >= n) break;  // warp-uniform
+                uint32_t v[32];
+                qt_ld32(tA + 32u * c, v);
+                if (rv) {
+                    uint16_t* dst = out + (size_t)row * n + col0;
+                    if (vec && col0 + 32 <= n) {
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            uint4 o;
+                            o.x = bf162_bits(__floats2bfloat162_rn(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])));
+                            o.y = bf162_bits(__floats2bfloat162_rn(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])));
+                            o.z = bf162_bits(__floats2bfloat162_rn(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])));
+                            o.w = bf162_bits(__floats2bfloat162_rn(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+                            *reinterpret_cast<uint4*>(dst + 8 * q) = o;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; e++) {
+                            if (col0 + e < n) {
+                                const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(v[e]));
+                                dst[e] = *reinterpret_cast<const uint16_t*>(&b);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    } else {
+        // ---------------------------------------------------------------- weight operand
+        const int bt = 32 * (warp - QT_BWARP0) + lane;  // weight row within the tile
+        const int nrow = n0 + bt;
+        const bool nv = nrow < n;
+        const uint8_t* wrow = wcodes + (size_t)(nv ? nrow : 0) * (k >> 2);
+        const uint16_t* srow = wsc + (size_t)(nv ? nrow : 0) * G;
+        uint8_t* bdst = bst + (bt >> 3) * 1024 + (bt & 7) * 16;
+        const __nv_bfloat162 m130 = bits_bf162(0xC302C302u);  // (-130, -130)
+        uint4 cp = make_uint4(0u, 0u, 0u, 0u), np = cp;
+        uint32_t cs = 0, ns = 0;
+        if (nv) {
+            cp = ldg_nc128(wrow);
+            cs = srow[0];
+        }
+        for (int s = 0; s < S; s++) {
+            const int st = s % QT_NS;
+            if (s + 1 < S && nv) {
+                np = ldg_nc128(wrow + 32 * ((s + 1) >> 1) + 16 * ((s + 1) & 1));
+                ns = srow[(s + 1) >> 1];
+            }
+            if (s >= QT_NS) {
+                if (!qt_wait_warp(&sempty[st], (uint32_t)((s / QT_NS) - 1) & 1u, abort)) break;
+            }
+            const __nv_bfloat162 d2 = bits_bf162(cs | (cs << 16));
+            uint8_t* dst = bdst + st * QT_BSTAGE;
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const uint32_t w = u4_get(cp, u);
+                uint32_t o[8];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+#pragma unroll
+                    for (int j = 0; j < 2; j++) {
+                        // codes of offsets 4u + j and 4u + j + 2 -> BF16 128 + c, then d * (c - 2)
+                        const uint32_t x = and_or(w >> (8 * j + 2 * i), 0x00030003u, 0x43004300u);
+                        o[2 * i + j] = bf162_bits(__hmul2(__hadd2(bits_bf162(x), m130), d2));
+                    }
+                }
+                *reinterpret_cast<uint4*>(dst + (2 * u) * 128) = make_uint4(o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<uint4*>(dst + (2 * u + 1) * 128) = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(&bfull[st]);
+            cp = np;
+            cs = ns;
+        }
+    }
+
+    qt_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        qt_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "n"(QT_TMEM_COLS));
+    }
+}
+
+static int qt_reserve_smem(size_t bytes, const char* who) {
+    static int cache[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 64) dev = 63;
+    if ((size_t)cache[dev] < bytes) {
+        if (cudaFuncSetAttribute((const void*)q2_mmq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)bytes) != cudaSuccess)
+            return fail(BQ_ERR_LAUNCH, "%s: cannot reserve %zu bytes of shared memory", who, bytes);
+        cache[dev] = (int)bytes;
+    }
+    return BQ_OK;
+}
+
+}  // namespace bq8
+
+using namespace bq8;
+
+extern "C" int q2_mmq_gemm(const void* act_q8, const bq_q2_weight* w, uint16_t* out, uint32_t m,
+                           bq_stream_t stream) {
+    const char* who = "q2_mmq_gemm";
+    int st = check_q2(w, who);
+    if (st) return st;
+    if (w->group != 128) return fail(BQ_ERR_INVALID, "%s: the MMQ route needs group size 128 (got %u)", who, w->group);
+    if (m == 0 || w->n == 0) return ok();
+    if (!out || !aligned16(out)) return fail(BQ_ERR_INVALID, "%s: out NULL or not 16-byte aligned", who);
+    if (w->k == 0) {
+        if (cudaMemsetAsync(out, 0, (size_t)m * w->n * 2, (cudaStream_t)stream) != cudaSuccess)
+            return fail(BQ_ERR_LAUNCH, "%s: memset failed", who);
+        return ok();
+    }
+    if (!act_q8 || !aligned16(act_q8)) return fail(BQ_ERR_INVALID, "%s: act_q8 NULL or not 16-byte aligned", who);
+    if (m > (1u << 24) || w->n > (1u << 24) || w->k > (1u << 24))
+        return fail(BQ_ERR_INVALID, "%s: shape too large", who);
+    const uint64_t kp = ((uint64_t)w->k + 255) / 256 * 256;
+    const uint8_t* codes = (const uint8_t*)act_q8;
+    const float* ds = (const float*)(codes + (uint64_t)m * kp);
+    const uint8_t* wcodes = (const uint8_t*)w->data;
+    const uint16_t* wsc = (const uint16_t*)(wcodes + (size_t)w->n * (w->k / 4));
+    const size_t smem = 1024 + (size_t)QT_NS * QT_BSTAGE + (3 * QT_NS + 1) * 8 + 16;
+    if ((st = qt_reserve_smem(smem, who))) return st;
+    const int ntn = (int)((w->n + QT_BN - 1) / QT_BN);
+    const uint64_t tiles = (uint64_t)ntn * ((m + QT_BM - 1) / QT_BM);
+    if (tiles > 0x7FFFFFFFull) return fail(BQ_ERR_INVALID, "%s: shape too large", who);
+    q2_mmq_tc_kernel<<<(unsigned)tiles, QT_THREADS, smem, (cudaStream_t)stream>>>(
+        codes, ds, (int)kp, wcodes, wsc, out, (int)m, (int)w->n, (int)w->k, ntn);
+    return check_launch(who);
+}

@@ -145,9 +145,12 @@ int ffn_q2_km(const uint16_t* x, const bq_q2_weight* gate, const bq_q2_weight* u
 int ffn_q2_km_noalloc(const uint16_t* x, const bq_q2_weight* gate, const bq_q2_weight* up, const bq_q2_weight* down,
                       uint16_t* out, uint32_t m, bq_stream_t stream);
 
-/* Q2_0 MMQ: out[m][n] = q8_1(act) @ Wdq^T with integer products per 32-value block and
- * fp32 rescaling, BF16 store.  act_q8 is quantize_act_q8_1's output for [m][w->k];
+/* Q2_0 MMQ: out[m][n] = q8_1(act) @ Wdq^T, i.e. sum_k (d_a q)[m][k] * (d_w (c - 2))[n][k],
+ * fp32 accumulation, BF16 store.  act_q8 is quantize_act_q8_1's output for [m][w->k];
  * w->group must be 128 (the page's MMQ condition).  Any m >= 1 and any n.
+ * Computed on the BF16 tensor cores: the weight operand d_w (c - 2) is exact in BF16 and
+ * each activation value d_a q enters as a pair of BF16 values whose sum equals it to
+ * 2^-17 relative.
  * Source: init_q2.rs, `qkvz_q2_prefill_gemm` (MMQ route, `q2_0_mmq_gemm`). */
 int q2_mmq_gemm(const void* act_q8, const bq_q2_weight* w, uint16_t* out, uint32_t m, bq_stream_t stream);
 
