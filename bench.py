@@ -339,12 +339,24 @@ def run_ours(args, rank, local, world):
 
 
 def measure_rows(args, dev, hbm_peak, bf16_peak):
-    import numpy as np
+    rows = {}
+    reps = max(5, min(args.steps, 50))
+    groups = set(args.rows.split(","))
+    if "gemv1024" in groups:
+        _rows_gemv1024(rows, reps, dev, hbm_peak)
+    if "ffn" in groups:
+        _rows_ffn(rows, reps, dev, hbm_peak)
+    if "prefill" in groups:
+        _rows_prefill(rows, reps, dev, hbm_peak, bf16_peak)
+    if "q4k" in groups:
+        _rows_q4k(rows, reps, dev)
+    return rows
+
+
+def _rows_gemv1024(rows, reps, dev, hbm_peak):
     import torch
     import bit_quantized_linear_q8_gb300 as B
     from bit_quantized_linear_q8_gb300 import synth
-    rows = {}
-    reps = max(5, min(args.steps, 50))
 
     # a1: 1024 x 1024 GEMV, m = 1 (latency-bound: 278,528 weight bytes)
     d = synth.q2_gemv_1024()
@@ -359,6 +371,12 @@ def measure_rows(args, dev, hbm_peak, bf16_peak):
                                "note": "512 distinct copies (143 MB) per graph; per-launch time includes graph gaps"}
     del copies, g
     torch.cuda.empty_cache()
+
+
+def _rows_ffn(rows, reps, dev, hbm_peak):
+    import torch
+    import bit_quantized_linear_q8_gb300 as B
+    from bit_quantized_linear_q8_gb300 import synth
 
     # a2-a4: packed-Q2 FFN decode chain (gate/up [17408, 5120], down [5120, 17408])
     d = synth.ffn_q2_decode()
@@ -394,6 +412,12 @@ def measure_rows(args, dev, hbm_peak, bf16_peak):
     del sets, ws, g
     torch.cuda.empty_cache()
 
+
+def _rows_prefill(rows, reps, dev, hbm_peak, bf16_peak):
+    import torch
+    import bit_quantized_linear_q8_gb300 as B
+    from bit_quantized_linear_q8_gb300 import synth
+
     # a5, a6, a8, a9: Q2 prefill projection
     d = synth.q2_prefill_weight()
     w = B.q2_pack(torch.from_numpy(d["codes"]).to(dev), _bf(d["scales"], dev))
@@ -414,12 +438,21 @@ def measure_rows(args, dev, hbm_peak, bf16_peak):
         rows["a5_q8_1_m%d" % m] = {"us": tq * 1e6, "GBps": qb / tq / 1e9, "frac_hbm": qb / tq / 1e9 / hbm_peak}
         rows["a6_q2_mmq_m%d" % m] = {"us": tm * 1e6, "TOPS": flops / tm / 1e12,
                                      "frac_bf16_dense_peak": flops / tm / 1e12 / bf16_peak,
-                                     "pipe": "mma.sync m16n8k32 s8.u8 (legacy warp MMA; sm_103a has no tcgen05 int8)"}
+                                     "tensor_pipe_frac": 2 * flops / tm / 1e12 / bf16_peak,
+                                     "pipe": "tcgen05.mma kind::f16 M128 N256 K16: exact BF16 weights d(c-2), q8_1 "
+                                             "activations as a hi/lo BF16 pair (2 MMAs per K16; sm_103a has no "
+                                             "tcgen05 int8)"}
         rows["a9_dequant_plus_cublas_m%d" % m] = {"us": (tg + rows["a8_dequant_16384x5120"]["us"] / 1e6) * 1e6,
                                                  "gemm_us": tg * 1e6, "TFLOPS_gemm": flops / tg / 1e12}
         del x, act, out
     del w, wd
     torch.cuda.empty_cache()
+
+
+def _rows_q4k(rows, reps, dev):
+    import torch
+    import bit_quantized_linear_q8_gb300 as B
+    from bit_quantized_linear_q8_gb300 import synth
 
     # a7: Q4_K MMQ FFN prefill (gate, up -> SiLU*mul -> down) at m = 2048
     try:
@@ -445,10 +478,10 @@ def measure_rows(args, dev, hbm_peak, bf16_peak):
         flops = 3 * 2.0 * m * hidden * inter
         rows["a7_q4k_ffn_prefill_m2048"] = {"us": t * 1e6, "TOPS_chain": flops / t / 1e12,
                                             "gate_gemm_us": tg * 1e6,
-                                            "gate_TOPS": 2.0 * m * hidden * inter / tg / 1e12}
+                                            "gate_TOPS": 2.0 * m * hidden * inter / tg / 1e12,
+                                            "pipe": "mma.sync m16n8k32 s8.u8 (legacy warp MMA)"}
     except Exception as e:  # reported, not hidden
         rows["a7_q4k_ffn_prefill_m2048"] = {"error": str(e)[:200]}
-    return rows
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -514,6 +547,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=16, help="distinct qkvz layer weights per step")
     ap.add_argument("--no-rows", action="store_true", help="headline only")
+    ap.add_argument("--rows", default="gemv1024,ffn,prefill,q4k",
+                    help="row groups to measure: gemv1024 (a1), ffn (a2-a4), prefill (a5, a6, a8, a9), q4k (a7)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)

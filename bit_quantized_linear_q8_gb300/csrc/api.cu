@@ -92,6 +92,21 @@ int make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t ro
     return BQ_OK;
 }
 
+int make_tmap_3d_u8(CUtensorMap* map, const void* base, const uint64_t (&dims)[3], const uint64_t (&strides)[2],
+                    const uint32_t (&box)[3], const char* who) {
+    PFN_encodeTiled fn = encode_fn();
+    if (!fn) return fail(BQ_ERR_UNSUPPORTED, "%s: cuTensorMapEncodeTiled unavailable from the driver", who);
+    const cuuint64_t gd[3] = {dims[0], dims[1], dims[2]};
+    const cuuint64_t gs[2] = {strides[0], strides[1]};
+    const cuuint32_t bx[3] = {box[0], box[1], box[2]};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), gd, gs, bx, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(BQ_ERR_INVALID, "%s: tensor map encoding failed (CUresult %d)", who, (int)r);
+    return BQ_OK;
+}
+
 }  // namespace bq8
 
 extern "C" {

@@ -37,6 +37,11 @@ int make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t row_bytes, uint
 int make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t row_elems, uint64_t rows,
                  uint64_t stride_bytes, uint32_t box_elems, uint32_t box_rows, bool swizzle128, const char* who);
 
+// 3-D tiled TMA descriptor over bytes: dims {d0, d1, d2}, byte strides of d1 and d2 (any
+// order, multiples of 16), box {b0, b1, b2} (b0 a multiple of 16), no swizzle.
+int make_tmap_3d_u8(CUtensorMap* map, const void* base, const uint64_t (&dims)[3], const uint64_t (&strides)[2],
+                    const uint32_t (&box)[3], const char* who);
+
 // Reads and clears each translation unit's device status word (nonzero after a bounded
 // wait gave up).
 unsigned int gemv_status_take();
@@ -152,6 +157,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
         ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 3-D TMA tile load global -> shared, completion counted on `bar` (bytes).
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
 }
 

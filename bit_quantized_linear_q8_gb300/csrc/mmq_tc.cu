@@ -20,13 +20,17 @@
 //    and four stages of the activation operand (A from tensor memory: lane = row, column j =
 //    K elements 2j, 2j+1; 32 columns hi + 32 columns lo per stage).  Shared memory holds four
 //    stages of the weight operand (256 x 64 BF16, no-swizzle K-major 8 x 16-byte core
-//    matrices).  No global scratch.
+//    matrices) and a five-step ring of the packed inputs.  No global scratch.
+//  * Warp 13 streams the packed inputs of each K step into the ring with TMA: the q8_1 codes
+//    (a [run][row][16 B] box, so that a warp reads 32 consecutive rows), the q8_1 (d, s)
+//    pairs and the 2-bit weight codes.  The group scales (one BF16 per 128 columns) are read
+//    one pack block ahead with plain loads.
 //  * Warp 0 allocates tensor memory; one lane issues M128 N256 K16 MMAs (8 per K step) and
 //    commits each step to the stage's `empty` barrier.
-//  * Warps 1-4 (one per tensor-memory lane quadrant, one activation row per thread) expand
-//    the q8_1 codes into the hi/lo operand with tcgen05.st, then run the epilogue
-//    (tcgen05.ld -> BF16 -> global).
-//  * Warps 5-12 (one weight row per thread) expand the 2-bit codes into shared memory.
+//  * Warps 1-8 (two per tensor-memory lane quadrant, one activation row per thread, each
+//    warp half of the step's words) expand the q8_1 codes into the hi/lo operand with
+//    tcgen05.st, then run the epilogue (tcgen05.ld -> BF16 -> global).
+//  * Warps 9-12 (two weight rows per thread) expand the 2-bit codes into shared memory.
 //  * K order inside a step: the 64 columns of step s are those of pack block s/2 with
 //    in-block offsets 32i + 16(s%2) + l (i = 0..3, l = 0..15), and 32-bit operand word
 //    q = 8u + 2i + j holds offsets (l = 4u + j, l = 4u + j + 2).  In the Q2 layout (byte l of a
@@ -52,16 +56,25 @@ unsigned int mmq_tc_status_take() {
 
 constexpr int QT_BM = 128;
 constexpr int QT_BN = 256;
-constexpr int QT_NS = 4;                         // K-step stages (tensor memory and shared memory)
-constexpr int QT_AWARP0 = 1;                     // warps 1..4: activation operand, epilogue
-constexpr int QT_BWARP0 = 5;                     // warps 5..12: weight operand
-constexpr int QT_THREADS = 13 * 32;
+constexpr int QT_NS = 4;                         // operand stages (tensor memory and shared memory)
+constexpr int QT_NR = 5;                         // ring stages of packed inputs
+constexpr int QT_AWARP0 = 1;                     // warps 1..8: activation operand, epilogue
+constexpr int QT_BWARP0 = 9;                     // warps 9..12: weight operand, two rows a thread
+constexpr int QT_PWARP = 13;                     // TMA producer
+constexpr int QT_THREADS = 14 * 32;
 constexpr uint32_t QT_BSTAGE = QT_BN * 64 * 2;   // 32 KB of weight operand per stage
+constexpr uint32_t QT_R_A = 0;                   // ring stage: q8_1 codes [4 runs][128 rows][16 B]
+constexpr uint32_t QT_R_D = 8192;                // (d, s) pairs [2][128 rows][16 B]
+constexpr uint32_t QT_R_B = 12288;               // weight codes [256 rows][16 B]
+constexpr uint32_t QT_RSTAGE = 16384;
 constexpr uint32_t QT_TMEM_COLS = 512;
 constexpr uint32_t QT_ACOL = 256;                // first column of the activation stages
 constexpr uint32_t QT_WAIT_LIMIT = 1u << 22;     // polls (~64 ns each) before a wait gives up
 static_assert(QT_ACOL + 64 * QT_NS <= QT_TMEM_COLS, "tensor memory budget");
-static_assert(QT_BWARP0 == QT_AWARP0 + 4 && QT_THREADS == (QT_BWARP0 + QT_BN / 32) * 32, "warp roles");
+static_assert(QT_BWARP0 == QT_AWARP0 + 8 && QT_PWARP == QT_BWARP0 + QT_BN / 64 && QT_THREADS == (QT_PWARP + 1) * 32,
+              "warp roles");
+constexpr size_t QT_SMEM = 1024 + (size_t)QT_NS * QT_BSTAGE + (size_t)QT_NR * QT_RSTAGE + (3 * QT_NS + 2 * QT_NR + 1) * 8 + 16;
+static_assert(QT_SMEM <= 227 * 1024, "shared memory budget");
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bit 4), A and B BF16 (bits 7-9,
 // 10-12), both K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
@@ -148,16 +161,21 @@ __device__ __forceinline__ uint32_t u4_get(const uint4& v, int u) {
     return u == 0 ? v.x : u == 1 ? v.y : u == 2 ? v.z : v.w;
 }
 
-__global__ void __launch_bounds__(QT_THREADS, 1)
-    q2_mmq_tc_kernel(const uint8_t* __restrict__ acodes, const float* __restrict__ ads, int kp,
-                     const uint8_t* __restrict__ wcodes, const uint16_t* __restrict__ wsc,
+// (Launch bounds of 512 threads keep ptxas at <= 128 registers: 14 warps put four warps on
+// one SM sub-partition, whose register file holds 16 K registers.)
+__global__ void __launch_bounds__(512, 1)
+    q2_mmq_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapD,
+                     const __grid_constant__ CUtensorMap mapB, const uint16_t* __restrict__ wsc,
                      uint16_t* __restrict__ out, int m, int n, int k, int ntn) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* bst = align1024(smem_raw);
-    uint64_t* afull = reinterpret_cast<uint64_t*>(bst + QT_NS * QT_BSTAGE);
+    uint8_t* ring = bst + QT_NS * QT_BSTAGE;
+    uint64_t* afull = reinterpret_cast<uint64_t*>(ring + QT_NR * QT_RSTAGE);
     uint64_t* bfull = afull + QT_NS;
     uint64_t* sempty = bfull + QT_NS;
-    uint64_t* accfull = sempty + QT_NS;
+    uint64_t* rfull = sempty + QT_NS;
+    uint64_t* rempty = rfull + QT_NR;
+    uint64_t* accfull = rempty + QT_NR;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(accfull + 1);
     volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
 
@@ -168,9 +186,13 @@ __global__ void __launch_bounds__(QT_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < QT_NS; s++) {
-            mbar_init(&afull[s], 4 * 32);
-            mbar_init(&bfull[s], 8 * 32);
+            mbar_init(&afull[s], 8 * 32);
+            mbar_init(&bfull[s], 4 * 32);
             mbar_init(&sempty[s], 1);
+        }
+        for (int r = 0; r < QT_NR; r++) {
+            mbar_init(&rfull[r], 1);
+            mbar_init(&rempty[r], 12);  // one arrival per consuming warp
         }
         mbar_init(accfull, 1);
         *abort = 0;
@@ -186,7 +208,23 @@ __global__ void __launch_bounds__(QT_THREADS, 1)
     qt_fence_after();
     const uint32_t tbase = *tslot;
 
-    if (warp == 0) {
+    if (warp == QT_PWARP) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            for (int s = 0; s < S; s++) {
+                const int r = s % QT_NR;
+                if (s >= QT_NR && !qt_wait(&rempty[r], (uint32_t)((s / QT_NR) - 1) & 1u, abort)) break;
+                const int pb = s >> 1, h = s & 1;
+                uint8_t* dst = ring + r * QT_RSTAGE;
+                mbar_arrive_expect_tx(&rfull[r], QT_RSTAGE);
+                tma_load_3d(dst + QT_R_A, &mapA, 16 * h, m0, 4 * pb, &rfull[r]);
+                tma_load_3d(dst + QT_R_D, &mapD, 0, m0, 2 * pb, &rfull[r]);
+                tma_load_2d(dst + QT_R_B, &mapB, 32 * pb + 16 * h, n0, &rfull[r]);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 0) {
+        // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             for (int s = 0; s < S; s++) {
                 const int st = s % QT_NS;
@@ -209,77 +247,66 @@ __global__ void __launch_bounds__(QT_THREADS, 1)
         __syncwarp();
     } else if (warp < QT_BWARP0) {
         // ---------------------------------------------------------------- activation operand
+        // Two warps per tensor-memory lane quadrant; warp half `hf` expands operand words
+        // 16hf .. 16hf + 15 of each step (u = 2hf, 2hf + 1) and later stores output columns
+        // 128hf .. 128hf + 127.
         const int qd = warp & 3;  // tensor-memory lane quadrant this warp may access
+        const int hf = (warp - QT_AWARP0) >> 2;
+        const int lrow = 32 * qd + lane;  // row within the tile
         const uint32_t tA = tbase + ((uint32_t)(32 * qd) << 16);
-        const int row = m0 + 32 * qd + lane;
-        const bool rv = row < m;
-        const uint8_t* arow = acodes + (size_t)(rv ? row : 0) * kp;
-        const float* drow = ads + (size_t)(rv ? row : 0) * (kp / 16);
-        uint4 cr[4], nr[4];
-        float cd[4], nd[4];
-        auto load = [&](int s, uint4 (&r)[4], float (&dd)[4]) {
-            const int pb = s >> 1, h = s & 1;
-            if (rv) {
-#pragma unroll
-                for (int i = 0; i < 4; i++) r[i] = ldg_nc128(arow + 128 * pb + 32 * i + 16 * h);
-                const uint4 p0 = ldg_nc128(drow + 8 * pb);
-                const uint4 p1 = ldg_nc128(drow + 8 * pb + 4);
-                dd[0] = __uint_as_float(p0.x);
-                dd[1] = __uint_as_float(p0.z);
-                dd[2] = __uint_as_float(p1.x);
-                dd[3] = __uint_as_float(p1.z);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    r[i] = make_uint4(0u, 0u, 0u, 0u);  // code 0 (after the 0x80 bias below), d = 0
-                    dd[i] = 0.f;
-                }
-            }
-        };
-        load(0, cr, cd);
         for (int s = 0; s < S; s++) {
-            const int st = s % QT_NS;
-            if (s + 1 < S) load(s + 1, nr, nd);
+            const int st = s % QT_NS, r = s % QT_NR;
+            if (!qt_wait_warp(&rfull[r], (uint32_t)(s / QT_NR) & 1u, abort)) break;
+            const uint8_t* rs = ring + r * QT_RSTAGE;
+            uint2 cr[4];
+            float cd[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+                cr[i] = *reinterpret_cast<const uint2*>(rs + QT_R_A + i * 2048 + lrow * 16 + 8 * hf);
+#pragma unroll
+            for (int jj = 0; jj < 2; jj++) {
+                const float4 p = *reinterpret_cast<const float4*>(rs + QT_R_D + jj * 2048 + lrow * 16);
+                cd[2 * jj] = p.x;
+                cd[2 * jj + 1] = p.z;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&rempty[r]);
             if (s >= QT_NS) {
                 if (!qt_wait_warp(&sempty[st], (uint32_t)((s / QT_NS) - 1) & 1u, abort)) break;
                 qt_fence_after();
             }
-            const uint32_t tcol = tA + QT_ACOL + 64u * st;
+            const uint32_t tcol = tA + QT_ACOL + 64u * st + 16u * hf;
 #pragma unroll
-            for (int u = 0; u < 4; u++) {
+            for (int uu = 0; uu < 2; uu++) {
                 uint32_t hw[8], lw[8];
 #pragma unroll
                 for (int i = 0; i < 4; i++) {
-                    const uint32_t wb = u4_get(cr[i], u) ^ 0x80808080u;
+                    const uint32_t wb = (uu ? cr[i].y : cr[i].x) ^ 0x80808080u;
                     // word 8u + 2i + j: offsets 4u + j (low half) and 4u + j + 2 (high half)
                     qt_split_pair(wb, 0x7540u, 0x7542u, cd[i], hw[2 * i], lw[2 * i]);
                     qt_split_pair(wb, 0x7541u, 0x7543u, cd[i], hw[2 * i + 1], lw[2 * i + 1]);
                 }
-                qt_st8(tcol + 8u * u, hw);
-                qt_st8(tcol + 32u + 8u * u, lw);
+                qt_st8(tcol + 8u * uu, hw);
+                qt_st8(tcol + 32u + 8u * uu, lw);
             }
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             qt_fence_before();
             mbar_arrive(&afull[st]);
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                cr[i] = nr[i];
-                cd[i] = nd[i];
-            }
         }
         // ---------------------------------------------------------------- epilogue
+        const int row = m0 + lrow;
         bool ok = mbar_wait(accfull, 0);
         ok = __all_sync(0xffffffffu, ok && !*abort) != 0;
         qt_fence_after();
         if (ok) {
             const bool vec = (n & 7) == 0;
 #pragma unroll 1
-            for (int c = 0; c < QT_BN / 32; c++) {
+            for (int c = 4 * hf; c < 4 * hf + 4; c++) {
                 const int col0 = n0 + 32 * c;
                 if (col0 >= n) break;  // warp-uniform
                 uint32_t v[32];
                 qt_ld32(tA + 32u * c, v);
-                if (rv) {
+                if (row < m) {
                     uint16_t* dst = out + (size_t)row * n + col0;
                     if (vec && col0 + 32 <= n) {
 #pragma unroll
@@ -305,50 +332,64 @@ __global__ void __launch_bounds__(QT_THREADS, 1)
         }
     } else {
         // ---------------------------------------------------------------- weight operand
-        const int bt = 32 * (warp - QT_BWARP0) + lane;  // weight row within the tile
-        const int nrow = n0 + bt;
-        const bool nv = nrow < n;
-        const uint8_t* wrow = wcodes + (size_t)(nv ? nrow : 0) * (k >> 2);
-        const uint16_t* srow = wsc + (size_t)(nv ? nrow : 0) * G;
-        uint8_t* bdst = bst + (bt >> 3) * 1024 + (bt & 7) * 16;
+        // Thread t expands weight rows t and t + 128 of the tile.
+        const int bt = 32 * (warp - QT_BWARP0) + lane;
         const __nv_bfloat162 m130 = bits_bf162(0xC302C302u);  // (-130, -130)
-        uint4 cp = make_uint4(0u, 0u, 0u, 0u), np = cp;
-        uint32_t cs = 0, ns = 0;
-        if (nv) {
-            cp = ldg_nc128(wrow);
-            cs = srow[0];
+        const uint16_t* srow[2];
+        bool nv[2];
+        uint32_t cs[2], ns[2];
+#pragma unroll
+        for (int r = 0; r < 2; r++) {
+            const int nr = n0 + bt + 128 * r;
+            nv[r] = nr < n;
+            srow[r] = wsc + (size_t)(nv[r] ? nr : 0) * G;
+            cs[r] = nv[r] ? srow[r][0] : 0u;
+            ns[r] = (nv[r] && G > 1) ? srow[r][1] : 0u;
         }
         for (int s = 0; s < S; s++) {
-            const int st = s % QT_NS;
-            if (s + 1 < S && nv) {
-                np = ldg_nc128(wrow + 32 * ((s + 1) >> 1) + 16 * ((s + 1) & 1));
-                ns = srow[(s + 1) >> 1];
+            const int st = s % QT_NS, rr = s % QT_NR;
+            const int pb = s >> 1;
+            if (s > 0 && (s & 1) == 0) {  // new pack block: its scale was loaded one block ago
+#pragma unroll
+                for (int r = 0; r < 2; r++) {
+                    cs[r] = ns[r];
+                    if (nv[r] && pb + 1 < G) ns[r] = srow[r][pb + 1];
+                }
             }
+            if (!qt_wait_warp(&rfull[rr], (uint32_t)(s / QT_NR) & 1u, abort)) break;
+            const uint8_t* rs = ring + rr * QT_RSTAGE + QT_R_B;
+            uint4 cp[2];
+#pragma unroll
+            for (int r = 0; r < 2; r++) cp[r] = *reinterpret_cast<const uint4*>(rs + (bt + 128 * r) * 16);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&rempty[rr]);
             if (s >= QT_NS) {
                 if (!qt_wait_warp(&sempty[st], (uint32_t)((s / QT_NS) - 1) & 1u, abort)) break;
             }
-            const __nv_bfloat162 d2 = bits_bf162(cs | (cs << 16));
-            uint8_t* dst = bdst + st * QT_BSTAGE;
 #pragma unroll
-            for (int u = 0; u < 4; u++) {
-                const uint32_t w = u4_get(cp, u);
-                uint32_t o[8];
+            for (int r = 0; r < 2; r++) {
+                const int row = bt + 128 * r;
+                const __nv_bfloat162 d2 = bits_bf162(cs[r] | (cs[r] << 16));
+                uint8_t* dst = bst + st * QT_BSTAGE + (row >> 3) * 1024 + (row & 7) * 16;
 #pragma unroll
-                for (int i = 0; i < 4; i++) {
+                for (int u = 0; u < 4; u++) {
+                    const uint32_t w = u4_get(cp[r], u);
+                    uint32_t o[8];
 #pragma unroll
-                    for (int j = 0; j < 2; j++) {
-                        // codes of offsets 4u + j and 4u + j + 2 -> BF16 128 + c, then d * (c - 2)
-                        const uint32_t x = and_or(w >> (8 * j + 2 * i), 0x00030003u, 0x43004300u);
-                        o[2 * i + j] = bf162_bits(__hmul2(__hadd2(bits_bf162(x), m130), d2));
+                    for (int i = 0; i < 4; i++) {
+#pragma unroll
+                        for (int j = 0; j < 2; j++) {
+                            // codes of offsets 4u + j and 4u + j + 2 -> BF16 128 + c, then d * (c - 2)
+                            const uint32_t x = and_or(w >> (8 * j + 2 * i), 0x00030003u, 0x43004300u);
+                            o[2 * i + j] = bf162_bits(__hmul2(__hadd2(bits_bf162(x), m130), d2));
+                        }
                     }
+                    *reinterpret_cast<uint4*>(dst + (2 * u) * 128) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4*>(dst + (2 * u + 1) * 128) = make_uint4(o[4], o[5], o[6], o[7]);
                 }
-                *reinterpret_cast<uint4*>(dst + (2 * u) * 128) = make_uint4(o[0], o[1], o[2], o[3]);
-                *reinterpret_cast<uint4*>(dst + (2 * u + 1) * 128) = make_uint4(o[4], o[5], o[6], o[7]);
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive(&bfull[st]);
-            cp = np;
-            cs = ns;
         }
     }
 
@@ -395,16 +436,23 @@ extern "C" int q2_mmq_gemm(const void* act_q8, const bq_q2_weight* w, uint16_t* 
     if (m > (1u << 24) || w->n > (1u << 24) || w->k > (1u << 24))
         return fail(BQ_ERR_INVALID, "%s: shape too large", who);
     const uint64_t kp = ((uint64_t)w->k + 255) / 256 * 256;
+    const uint64_t k = w->k, n = w->n;
     const uint8_t* codes = (const uint8_t*)act_q8;
-    const float* ds = (const float*)(codes + (uint64_t)m * kp);
+    const uint8_t* ds = codes + (uint64_t)m * kp;
     const uint8_t* wcodes = (const uint8_t*)w->data;
-    const uint16_t* wsc = (const uint16_t*)(wcodes + (size_t)w->n * (w->k / 4));
-    const size_t smem = 1024 + (size_t)QT_NS * QT_BSTAGE + (3 * QT_NS + 1) * 8 + 16;
-    if ((st = qt_reserve_smem(smem, who))) return st;
-    const int ntn = (int)((w->n + QT_BN - 1) / QT_BN);
+    const uint16_t* wsc = (const uint16_t*)(wcodes + (size_t)n * (k / 4));
+    CUtensorMap mA, mD, mB;
+    // q8_1 codes as [kp/32 chunks][m rows][32 B]: box {16 B, 128 rows, 4 chunks}
+    if ((st = make_tmap_3d_u8(&mA, codes, {32, m, kp / 32}, {kp, 32}, {16, QT_BM, 4}, who))) return st;
+    // (d, s) pairs as [kp/64 pair-pairs][m rows][16 B]: box {16 B, 128 rows, 2}
+    if ((st = make_tmap_3d_u8(&mD, ds, {16, m, kp / 64}, {kp / 4, 16}, {16, QT_BM, 2}, who))) return st;
+    // weight codes [n rows][k/4 B]: box {16 B, 256 rows}
+    if ((st = make_tmap_2d_u8(&mB, wcodes, k / 4, n, k / 4, 16, QT_BN, false, who))) return st;
+    if ((st = qt_reserve_smem(QT_SMEM, who))) return st;
+    const int ntn = (int)((n + QT_BN - 1) / QT_BN);
     const uint64_t tiles = (uint64_t)ntn * ((m + QT_BM - 1) / QT_BM);
     if (tiles > 0x7FFFFFFFull) return fail(BQ_ERR_INVALID, "%s: shape too large", who);
-    q2_mmq_tc_kernel<<<(unsigned)tiles, QT_THREADS, smem, (cudaStream_t)stream>>>(
-        codes, ds, (int)kp, wcodes, wsc, out, (int)m, (int)w->n, (int)w->k, ntn);
+    q2_mmq_tc_kernel<<<(unsigned)tiles, QT_THREADS, QT_SMEM, (cudaStream_t)stream>>>(mA, mD, mB, wsc, out, (int)m,
+                                                                                   (int)n, (int)k, ntn);
     return check_launch(who);
 }
