@@ -28,15 +28,17 @@
 //  * Warp 0 allocates tensor memory; one lane issues M128 N256 K16 MMAs (8 per K step) and
 //    commits each step to the stage's `empty` barrier.
 //  * Warps 1-8 (two per tensor-memory lane quadrant, one activation row per thread, each
-//    warp half of the step's words) expand the q8_1 codes into the hi/lo operand with
-//    tcgen05.st, then run the epilogue (tcgen05.ld -> BF16 -> global).
+//    warp two of the step's four 16-byte code runs) expand the q8_1 codes into the hi/lo
+//    operand with tcgen05.st, then run the epilogue (tcgen05.ld -> BF16 -> global).
 //  * Warps 9-12 (two weight rows per thread) expand the 2-bit codes into shared memory.
 //  * K order inside a step: the 64 columns of step s are those of pack block s/2 with
 //    in-block offsets 32i + 16(s%2) + l (i = 0..3, l = 0..15), and 32-bit operand word
-//    q = 8u + 2i + j holds offsets (l = 4u + j, l = 4u + j + 2).  In the Q2 layout (byte l of a
-//    pack block holds the codes of offsets 32i + l in bits 2i) those two codes sit 16 bits
-//    apart in one 32-bit word of packed codes, so one shift and one LOP3 place a pair of codes
-//    into a BF16 pair.  Both operands use this order, so the contraction is unchanged.
+//    q = 16(i/2) + 4u + 2(i%2) + j holds offsets (l = 4u + j, l = 4u + j + 2).  In the Q2
+//    layout (byte l of a pack block holds the codes of offsets 32i + l in bits 2i) those two
+//    codes sit 16 bits apart in one 32-bit word of packed codes, so a mask and one LOP3 place
+//    a pair of codes into a BF16 pair; the activation warp that owns runs i = 2hf, 2hf + 1
+//    writes the contiguous words 16hf .. 16hf + 15.  Both operands use this order, so the
+//    contraction is unchanged.
 //  * Every wait is bounded; a wait that gives up raises the CTA's abort flag and the status
 //    word, and the kernel winds down (it still waits for its own MMAs before freeing tensor
 //    memory).
@@ -69,7 +71,7 @@ constexpr uint32_t QT_R_B = 12288;               // weight codes [256 rows][16 B
 constexpr uint32_t QT_RSTAGE = 16384;
 constexpr uint32_t QT_TMEM_COLS = 512;
 constexpr uint32_t QT_ACOL = 256;                // first column of the activation stages
-constexpr uint32_t QT_WAIT_LIMIT = 1u << 22;     // polls (~64 ns each) before a wait gives up
+constexpr uint32_t QT_WAIT_LIMIT = 1u << 20;     // try_waits before a wait gives up (0.05-4 s)
 static_assert(QT_ACOL + 64 * QT_NS <= QT_TMEM_COLS, "tensor memory budget");
 static_assert(QT_BWARP0 == QT_AWARP0 + 8 && QT_PWARP == QT_BWARP0 + QT_BN / 64 && QT_THREADS == (QT_PWARP + 1) * 32,
               "warp roles");
@@ -110,6 +112,15 @@ __device__ __forceinline__ void qt_st8(uint32_t taddr, const uint32_t (&r)[8]) {
                  : "memory");
 }
 
+__device__ __forceinline__ void qt_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
 __device__ __forceinline__ void qt_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -123,12 +134,25 @@ __device__ __forceinline__ void qt_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// One mbarrier.try_wait: the warp may be suspended in hardware until the phase completes or
+// a system-dependent time limit (microseconds) passes; true once phase `parity` completed.
+__device__ __forceinline__ bool qt_try(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // Bounded wait that also gives up as soon as another thread of the CTA has raised `abort`.
+// (Every step's waits here last microseconds, so a suspending try_wait costs the pipeline
+// nothing and frees issue slots that polling would take.)
 __device__ __forceinline__ bool qt_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
     for (uint32_t it = 0; it < QT_WAIT_LIMIT; it++) {
-        if (mbar_test(bar, parity)) return true;
+        if (qt_try(bar, parity)) return true;
         if (*abort) return false;
-        __nanosleep(32);
     }
     *abort = 1;
     atomicOr(&g_mmq_tc_status, 1u);
@@ -155,6 +179,11 @@ __device__ __forceinline__ void qt_split_pair(uint32_t wb, uint32_t sel0, uint32
     const float2 h = make_float2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xFFFF0000u));
     const float2 r = __fadd2_rn(v, make_float2(-h.x, -h.y));
     lo = bf162_bits(__floats2bfloat162_rn(r.x, r.y));
+}
+
+// -(128 + 2 * 4^f) as a BF16 pair: -130, -136, -160.
+__device__ __forceinline__ __nv_bfloat162 qt_m_off(int f) {
+    return bits_bf162(f == 0 ? 0xC302C302u : f == 1 ? 0xC308C308u : 0xC320C320u);
 }
 
 __device__ __forceinline__ uint32_t u4_get(const uint4& v, int u) {
@@ -247,9 +276,9 @@ __global__ void __launch_bounds__(512, 1)
         __syncwarp();
     } else if (warp < QT_BWARP0) {
         // ---------------------------------------------------------------- activation operand
-        // Two warps per tensor-memory lane quadrant; warp half `hf` expands operand words
-        // 16hf .. 16hf + 15 of each step (u = 2hf, 2hf + 1) and later stores output columns
-        // 128hf .. 128hf + 127.
+        // Two warps per tensor-memory lane quadrant; warp half `hf` expands code runs
+        // i = 2hf, 2hf + 1 (operand words 16hf .. 16hf + 15) of each step and later stores
+        // output columns 128hf .. 128hf + 127.
         const int qd = warp & 3;  // tensor-memory lane quadrant this warp may access
         const int hf = (warp - QT_AWARP0) >> 2;
         const int lrow = 32 * qd + lane;  // row within the tile
@@ -258,37 +287,32 @@ __global__ void __launch_bounds__(512, 1)
             const int st = s % QT_NS, r = s % QT_NR;
             if (!qt_wait_warp(&rfull[r], (uint32_t)(s / QT_NR) & 1u, abort)) break;
             const uint8_t* rs = ring + r * QT_RSTAGE;
-            uint2 cr[4];
-            float cd[4];
+            uint4 cr[2];
 #pragma unroll
-            for (int i = 0; i < 4; i++)
-                cr[i] = *reinterpret_cast<const uint2*>(rs + QT_R_A + i * 2048 + lrow * 16 + 8 * hf);
-#pragma unroll
-            for (int jj = 0; jj < 2; jj++) {
-                const float4 p = *reinterpret_cast<const float4*>(rs + QT_R_D + jj * 2048 + lrow * 16);
-                cd[2 * jj] = p.x;
-                cd[2 * jj + 1] = p.z;
-            }
+            for (int ii = 0; ii < 2; ii++)
+                cr[ii] = *reinterpret_cast<const uint4*>(rs + QT_R_A + (2 * hf + ii) * 2048 + lrow * 16);
+            const float4 dp = *reinterpret_cast<const float4*>(rs + QT_R_D + hf * 2048 + lrow * 16);
+            const float cd[2] = {dp.x, dp.z};  // d of q8_1 blocks 4(s/2) + 2hf, + 1
             __syncwarp();
             if (lane == 0) mbar_arrive(&rempty[r]);
             if (s >= QT_NS) {
                 if (!qt_wait_warp(&sempty[st], (uint32_t)((s / QT_NS) - 1) & 1u, abort)) break;
                 qt_fence_after();
             }
-            const uint32_t tcol = tA + QT_ACOL + 64u * st + 16u * hf;
+            uint32_t hw[16], lw[16];
 #pragma unroll
-            for (int uu = 0; uu < 2; uu++) {
-                uint32_t hw[8], lw[8];
+            for (int u = 0; u < 4; u++) {
 #pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    const uint32_t wb = (uu ? cr[i].y : cr[i].x) ^ 0x80808080u;
-                    // word 8u + 2i + j: offsets 4u + j (low half) and 4u + j + 2 (high half)
-                    qt_split_pair(wb, 0x7540u, 0x7542u, cd[i], hw[2 * i], lw[2 * i]);
-                    qt_split_pair(wb, 0x7541u, 0x7543u, cd[i], hw[2 * i + 1], lw[2 * i + 1]);
+                for (int ii = 0; ii < 2; ii++) {
+                    const uint32_t wb = u4_get(cr[ii], u) ^ 0x80808080u;
+                    // word 16hf + 4u + 2ii + j: offsets 4u + j (low half) and 4u + j + 2 (high half)
+                    qt_split_pair(wb, 0x7540u, 0x7542u, cd[ii], hw[4 * u + 2 * ii], lw[4 * u + 2 * ii]);
+                    qt_split_pair(wb, 0x7541u, 0x7543u, cd[ii], hw[4 * u + 2 * ii + 1], lw[4 * u + 2 * ii + 1]);
                 }
-                qt_st8(tcol + 8u * uu, hw);
-                qt_st8(tcol + 32u + 8u * uu, lw);
             }
+            const uint32_t tcol = tA + QT_ACOL + 64u * st + 16u * hf;
+            qt_st16(tcol, hw);
+            qt_st16(tcol + 32u, lw);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             qt_fence_before();
             mbar_arrive(&afull[st]);
@@ -334,7 +358,6 @@ __global__ void __launch_bounds__(512, 1)
         // ---------------------------------------------------------------- weight operand
         // Thread t expands weight rows t and t + 128 of the tile.
         const int bt = 32 * (warp - QT_BWARP0) + lane;
-        const __nv_bfloat162 m130 = bits_bf162(0xC302C302u);  // (-130, -130)
         const uint16_t* srow[2];
         bool nv[2];
         uint32_t cs[2], ns[2];
@@ -369,23 +392,32 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
             for (int r = 0; r < 2; r++) {
                 const int row = bt + 128 * r;
-                const __nv_bfloat162 d2 = bits_bf162(cs[r] | (cs[r] << 16));
+                // Field i of a code byte (bits 2i, 2i + 1; i = 0..2 in place, i = 3 shifted to
+                // i = 2) masked into the mantissa of 128 gives 128 + c 4^i; subtracting
+                // 128 + 2 4^i and multiplying by d 4^-i gives d (c - 2), every step exact.
+                const __nv_bfloat162 d0 = bits_bf162(cs[r] | (cs[r] << 16));
+                const __nv_bfloat162 dsc[3] = {d0, __hmul2(d0, bits_bf162(0x3E803E80u)),   // d / 4
+                                               __hmul2(d0, bits_bf162(0x3D803D80u))};      // d / 16
                 uint8_t* dst = bst + st * QT_BSTAGE + (row >> 3) * 1024 + (row & 7) * 16;
 #pragma unroll
                 for (int u = 0; u < 4; u++) {
-                    const uint32_t w = u4_get(cp[r], u);
+                    const uint32_t w0 = u4_get(cp[r], u);
+                    const uint32_t w1 = __byte_perm(w0, 0u, 0x4341u);  // bytes 1, 3 -> 0, 2
                     uint32_t o[8];
 #pragma unroll
                     for (int i = 0; i < 4; i++) {
 #pragma unroll
                         for (int j = 0; j < 2; j++) {
-                            // codes of offsets 4u + j and 4u + j + 2 -> BF16 128 + c, then d * (c - 2)
-                            const uint32_t x = and_or(w >> (8 * j + 2 * i), 0x00030003u, 0x43004300u);
-                            o[2 * i + j] = bf162_bits(__hmul2(__hadd2(bits_bf162(x), m130), d2));
+                            // codes of offsets 4u + j and 4u + j + 2
+                            const uint32_t wj = j ? w1 : w0;
+                            const int f = i < 3 ? i : 2;
+                            const uint32_t x = and_or(i < 3 ? wj : wj >> 2, 0x00030003u << (2 * f), 0x43004300u);
+                            o[2 * i + j] = bf162_bits(__hmul2(__hadd2(bits_bf162(x), qt_m_off(f)), dsc[f]));
                         }
                     }
-                    *reinterpret_cast<uint4*>(dst + (2 * u) * 128) = make_uint4(o[0], o[1], o[2], o[3]);
-                    *reinterpret_cast<uint4*>(dst + (2 * u + 1) * 128) = make_uint4(o[4], o[5], o[6], o[7]);
+                    // words 4u + 2(i%2) + j of core matrix u (i < 2) and 4 + u (i >= 2)
+                    *reinterpret_cast<uint4*>(dst + u * 128) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4*>(dst + (4 + u) * 128) = make_uint4(o[4], o[5], o[6], o[7]);
                 }
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
