@@ -29,7 +29,10 @@
 //    are independent.
 //  * Work split: CTA c takes a contiguous range of <= T row tiles (grid = SM count when
 //    possible, so every SM streams the same number of rows); the warps' partial sums are
-//    reduced through shared memory and stored as BF16.
+//    reduced through shared memory and stored as BF16.  When the rows are too few to give
+//    every SM about seven tiles (the down projection: 320 tiles of a long k), a cluster of
+//    S CTAs shares a row range, each streaming 1/S of the chunks, and the leader adds the
+//    members' partial sums through distributed shared memory before the BF16 store.
 #include "common.cuh"
 
 namespace bq8 {
@@ -118,6 +121,35 @@ struct GemvStage {
     __host__ __device__ static int bytes(int m) { return CODES + 4 * m * GEMV_XBOX * 2; }
 };
 
+// Scale groups per row a CTA stages: all of them, or at most those touched by one K part.
+__host__ __device__ inline int gemv_staged_groups(int k, int group, int ksplit) {
+    const int G = k / group;
+    if (ksplit <= 1) return G;
+    const int nch_all = ((k >> 7) + GEMV_PBLK - 1) / GEMV_PBLK;
+    const int maxch = (nch_all + ksplit - 1) / ksplit;
+    const int gs = (maxch * GEMV_PBLK * 128 + group - 1) / group + 1;
+    return gs < G ? gs : G;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// fp32 at the same shared-memory offset as `local` in CTA `rank` of the cluster.
+__device__ __forceinline__ float ld_cluster_f32(const void* local, uint32_t rank) {
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+    return v;
+}
+
 // Requests chunk c into stage s: the codes of the CTA's rows (one box per 128-byte half;
 // `tmap` has a box of exactly nt*16 rows) and the chunk's activation columns.
 template <int T>
@@ -149,37 +181,56 @@ template <int T>
 __global__ void __launch_bounds__(GEMV_THREADS, 1)
     q2_gemv_kernel(const __grid_constant__ CUtensorMap tmap_full, const __grid_constant__ CUtensorMap tmap_less,
                    const __grid_constant__ CUtensorMap xmap, const uint16_t* __restrict__ scales,
-                   uint16_t* __restrict__ y, int m, int n, int k, int group, int ntiles, int nstages) {
+                   uint16_t* __restrict__ y, int m, int n, int k, int group, int ntiles, int nstages, int ksplit) {
     constexpr int TQ = T;  // tiles per warp
     extern __shared__ uint8_t smem_raw[];
     uint8_t* stages = align1024(smem_raw);
     const int stage_bytes = (GemvStage<T>::bytes(m) + 1023) & ~1023;
     const int G = k / group;
-    // the CTA's rows of the BF16 scale plane, from byte s_lo of the plane on
+    // the CTA's scales (see below), then the barriers
     uint8_t* scs = stages + nstages * stage_bytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(scs + (((size_t)32 * T * G + 32 + 15) & ~size_t(15)));
+    uint64_t* full =
+        reinterpret_cast<uint64_t*>(scs + (((size_t)32 * T * gemv_staged_groups(k, group, ksplit) + 32 + 15) & ~size_t(15)));
     uint64_t* sfull = full + GEMV_MAX_STAGES;                                   // scales landed
     uint32_t* released = reinterpret_cast<uint32_t*>(sfull + 1);               // per stage: warps done with it
     int* issued = reinterpret_cast<int*>(released + GEMV_MAX_STAGES);          // per stage: last chunk requested
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
-    const int tile0 = (int)((int64_t)blockIdx.x * ntiles / gridDim.x);
-    const int nt = (int)((int64_t)(blockIdx.x + 1) * ntiles / gridDim.x) - tile0;
+    // row group and K part (cluster rank) of this CTA
+    const int rank = ksplit > 1 ? (int)cluster_rank() : 0;
+    const int rg = blockIdx.x / ksplit, ngroups = gridDim.x / ksplit;
+    const int tile0 = (int)((int64_t)rg * ntiles / ngroups);
+    const int nt = (int)((int64_t)(rg + 1) * ntiles / ngroups) - tile0;
     const int r0 = tile0 * 16;
     const int P = k >> 7;
-    const int nch = (P + GEMV_PBLK - 1) / GEMV_PBLK;
+    const int nch_all = (P + GEMV_PBLK - 1) / GEMV_PBLK;
+    const int c_lo = rank * nch_all / ksplit;                 // this CTA's chunks: [c_lo, c_lo + nch)
+    const int nch = (rank + 1) * nch_all / ksplit - c_lo;
     const int pre = nch < nstages ? nch : nstages;
     const CUtensorMap* tmap = nt == T ? &tmap_full : &tmap_less;
-    // scale bytes of rows r0 .. r0 + rows: [s_lo, s_hi) by one bulk copy, the rest (at most 14
-    // bytes at the end of the plane) by plain loads
     const int rows = min(16 * nt, n - r0);
     const uint8_t* splane = reinterpret_cast<const uint8_t*>(scales);
-    const int64_t s_lo = ((int64_t)r0 * G * 2) & ~int64_t(15), s_end = (int64_t)(r0 + rows) * G * 2;
-    int64_t s_hi = (s_end + 15) & ~int64_t(15);
-    const int64_t plane16 = ((int64_t)n * G * 2) & ~int64_t(15);
-    if (s_hi > plane16) s_hi = plane16;
-    if (s_hi < s_lo) s_hi = s_lo;
+    // Scales in shared memory, [row][Gs] BF16 from group g_lo on.  Whole rows (ksplit == 1):
+    // bytes [s_lo, s_hi) of the plane by one bulk copy, the rest (at most 14 bytes at the end
+    // of the plane) by plain loads.  A K part (ksplit > 1): its groups only, by one bulk copy
+    // per row when the row pieces are 16-byte aligned (G, g_lo, Gs multiples of 8), else by
+    // plain loads.
+    const int g_lo = ksplit > 1 ? (int)(((int64_t)c_lo * GEMV_PBLK * 128) / group) : 0;
+    const int g_hi = ksplit > 1 ? min(G, (int)(((int64_t)(c_lo + nch) * GEMV_PBLK * 128 + group - 1) / group)) : G;
+    const int Gs = g_hi - g_lo;
+    int64_t s_lo = 0, s_hi = 0, s_end = 0;
+    if (ksplit == 1) {
+        s_lo = ((int64_t)r0 * G * 2) & ~int64_t(15);
+        s_end = (int64_t)(r0 + rows) * G * 2;
+        s_hi = (s_end + 15) & ~int64_t(15);
+        const int64_t plane16 = ((int64_t)n * G * 2) & ~int64_t(15);
+        if (s_hi > plane16) s_hi = plane16;
+        if (s_hi < s_lo) s_hi = s_lo;
+    }
+    const uint16_t* sbase = ksplit == 1 ? reinterpret_cast<const uint16_t*>(scs + ((int64_t)r0 * G * 2 - s_lo))
+                                        : reinterpret_cast<const uint16_t*>(scs);
+    const bool srow_bulk = ksplit > 1 && (G & 7) == 0 && (g_lo & 7) == 0 && (Gs & 7) == 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nstages; s++) {
@@ -191,16 +242,41 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1)
         fence_barrier_init();
         // weights first: they do not depend on the kernel launched before this one
         // (programmatic dependent launch); the activations once that kernel has finished
-        for (int c = 0; c < pre; c++) gemv_issue_codes<T>(stages, stage_bytes, full, tmap, c, c, nt, r0, m);
-        mbar_arrive_expect_tx(sfull, (uint32_t)(s_hi - s_lo));
-        if (s_hi > s_lo) bulk_load(scs, splane + s_lo, (uint32_t)(s_hi - s_lo), sfull);
+        for (int c = 0; c < pre; c++) gemv_issue_codes<T>(stages, stage_bytes, full, tmap, c_lo + c, c, nt, r0, m);
+        if (srow_bulk) {
+            mbar_arrive_expect_tx(sfull, (uint32_t)(rows * Gs * 2));
+            for (int rr = 0; rr < rows; rr++)
+                bulk_load(scs + (size_t)rr * Gs * 2, scales + (size_t)(r0 + rr) * G + g_lo, (uint32_t)(Gs * 2), sfull);
+        } else {
+            mbar_arrive_expect_tx(sfull, (uint32_t)(s_hi - s_lo));
+            if (s_hi > s_lo) bulk_load(scs, splane + s_lo, (uint32_t)(s_hi - s_lo), sfull);
+        }
         asm volatile("griddepcontrol.wait;" ::: "memory");
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-        for (int c = 0; c < pre; c++) gemv_issue_x<T>(stages, stage_bytes, full, &xmap, c, c, m);
+        for (int c = 0; c < pre; c++) gemv_issue_x<T>(stages, stage_bytes, full, &xmap, c_lo + c, c, m);
     }
-    if (threadIdx.x == 32)  // scale bytes past the bulk copy
-        for (int64_t o = s_hi; o < s_end; o += 2)
-            *reinterpret_cast<uint16_t*>(scs + (o - s_lo)) = __ldg(reinterpret_cast<const uint16_t*>(splane + o));
+    if (ksplit == 1) {
+        if (threadIdx.x == 32)  // scale bytes past the bulk copy
+            for (int64_t o = s_hi; o < s_end; o += 2)
+                *reinterpret_cast<uint16_t*>(scs + (o - s_lo)) = __ldg(reinterpret_cast<const uint16_t*>(splane + o));
+    } else if (!srow_bulk) {  // batches of eight loads in flight per thread
+        uint16_t* sd = reinterpret_cast<uint16_t*>(scs);
+        const int total = rows * Gs;
+        for (int base = threadIdx.x; base < total; base += 8 * (int)blockDim.x) {
+            uint16_t v[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                const int i = base + e * (int)blockDim.x;
+                const int rr = i / Gs, gg = i - rr * Gs;
+                v[e] = i < total ? __ldg(scales + (size_t)(r0 + rr) * G + g_lo + gg) : (uint16_t)0;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                const int i = base + e * (int)blockDim.x;
+                if (i < total) sd[i] = v[e];
+            }
+        }
+    }
     __syncthreads();
 
     bool failed = false;
@@ -215,7 +291,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1)
     const uint32_t one = 0x3F803F80u;
     for (int c = 0; c < nch; c++) {
         const int s = c % nstages;
-        const int p = c * GEMV_PBLK + pb;
+        const int p = (c_lo + c) * GEMV_PBLK + pb;
         if (!mbar_wait(&full[s], (c / nstages) & 1)) {
             failed = true;
             break;
@@ -269,12 +345,12 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1)
                 break;
             }
             // scales of rows 16q + g and 16q + g + 8 (zero for tiles past nt)
-            const uint16_t* sr = reinterpret_cast<const uint16_t*>(scs + ((int64_t)(r0 + g) * G * 2 - s_lo)) + gi;
+            const uint16_t* sr = sbase + g * Gs + (gi - g_lo);
 #pragma unroll
             for (int q = 0; q < TQ; q++) {
                 const bool v = q < nt;
-                const float da = v ? bf16_bits_to_f32(sr[(16 * q) * G]) : 0.f;
-                const float db = v ? bf16_bits_to_f32(sr[(16 * q + 8) * G]) : 0.f;
+                const float da = v ? bf16_bits_to_f32(sr[(16 * q) * Gs]) : 0.f;
+                const float db = v ? bf16_bits_to_f32(sr[(16 * q + 8) * Gs]) : 0.f;
                 tot[q][0] = fmaf(da, acc[q][0], tot[q][0]);
                 tot[q][1] = fmaf(da, acc[q][1], tot[q][1]);
                 tot[q][2] = fmaf(db, acc[q][2], tot[q][2]);
@@ -292,7 +368,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1)
                 if (cn < nch) {
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     issued[s] = cn;
-                    gemv_issue<T>(stages, stage_bytes, full, tmap, &xmap, cn, s, nt, r0, m);
+                    gemv_issue<T>(stages, stage_bytes, full, tmap, &xmap, c_lo + cn, s, nt, r0, m);
                 }
             }
         }
@@ -317,6 +393,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1)
     }
     __syncthreads();
     const int per_col = nt * 16;
+    float* part = red + GEMV_PBLK * T * 160;  // [m][16 T]: this CTA's sums (K parts only)
     for (int o = threadIdx.x; o < per_col * m; o += blockDim.x) {
         const int j = o / per_col, rem = o % per_col, tau = rem >> 4, r = rem & 15;
         const int row = r0 + tau * 16 + r;
@@ -325,21 +402,40 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1)
         float sum = 0.f;
 #pragma unroll
         for (int w = 0; w < GEMV_PBLK; w++) sum += red[(w * T + tau) * 160 + ln * 5 + e];
-        const __nv_bfloat16 bv = __float2bfloat16_rn(sum);
-        y[(size_t)j * n + row] = *reinterpret_cast<const uint16_t*>(&bv);
+        if (ksplit > 1) {
+            part[j * 16 * T + rem] = sum;
+        } else {
+            const __nv_bfloat16 bv = __float2bfloat16_rn(sum);
+            y[(size_t)j * n + row] = *reinterpret_cast<const uint16_t*>(&bv);
+        }
+    }
+    if (ksplit > 1) {
+        cluster_sync_all();  // every member's partial sums are in its shared memory
+        if (rank == 0) {
+            for (int o = threadIdx.x; o < per_col * m; o += blockDim.x) {
+                const int j = o / per_col, rem = o % per_col;
+                const int row = r0 + rem;
+                if (row >= n) continue;
+                float sum = part[j * 16 * T + rem];
+                for (int q = 1; q < ksplit; q++) sum += ld_cluster_f32(&part[j * 16 * T + rem], (uint32_t)q);
+                const __nv_bfloat16 bv = __float2bfloat16_rn(sum);
+                y[(size_t)j * n + row] = *reinterpret_cast<const uint16_t*>(&bv);
+            }
+        }
+        cluster_sync_all();  // members keep their shared memory until the leader has read it
     }
 }
 
 template <int T>
 static int launch_t(const uint8_t* codes, const CUtensorMap& xmap, const uint16_t* scales, uint16_t* y, int m,
-                    int n, int k, int group, int ntiles, int ncta, cudaStream_t stream, const char* who) {
+                    int n, int k, int group, int ntiles, int ncta, int ksplit, cudaStream_t stream, const char* who) {
     static int configured_smem[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 64) dev = 63;
-    const int G = k / group;
+    const int Gst = gemv_staged_groups(k, group, ksplit);
     const size_t stage = ((size_t)GemvStage<T>::bytes(m) + 1023) & ~size_t(1023);
-    const size_t fixed = 1024 + (((size_t)32 * T * G + 32 + 15) & ~size_t(15)) + (GEMV_MAX_STAGES * 2 + 1) * 8 + 16;
+    const size_t fixed = 1024 + (((size_t)32 * T * Gst + 32 + 15) & ~size_t(15)) + (GEMV_MAX_STAGES * 2 + 1) * 8 + 16;
     // At most ~112 KB where two stages allow it, so the CTA of the next launch (programmatic
     // dependent launch) can share the SM and start its weight copies before this one ends.
     int nstages = GEMV_MAX_STAGES;
@@ -362,13 +458,17 @@ static int launch_t(const uint8_t* codes, const CUtensorMap& xmap, const uint16_
     cfg.blockDim = dim3(GEMV_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;  // the K parts of a row range
+    attr[1].val.clusterDim.x = (unsigned)ksplit;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = ksplit > 1 ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, q2_gemv_kernel<T>, map_full, map_less, xmap, scales, y, m, n, k, group, ntiles,
-                           nstages) != cudaSuccess)
+                           nstages, ksplit) != cudaSuccess)
         return check_launch(who);
     return BQ_OK;
 }
@@ -382,11 +482,28 @@ static int launch_q2_gemv_mma(const uint16_t* x, const bq_q2_weight* w, uint16_t
     while (tmax > 1 && (size_t)32 * tmax * G > 96 * 1024) tmax--;
     if ((size_t)32 * tmax * G > 96 * 1024)
         return fail(BQ_ERR_INVALID, "%s: k/group = %d groups per row is too many", who, G);
-    int ncta = ntiles < sm_count() ? ntiles : sm_count();
+    const int sms = sm_count();
+    int ncta = ntiles < sms ? ntiles : sms;
     int T = (ntiles + ncta - 1) / ncta;
     if (T > tmax) {
         ncta = (ntiles + tmax - 1) / tmax;
         T = (ntiles + ncta - 1) / ncta;  // every CTA then gets T or T - 1 tiles
+    }
+    // Too few rows for about seven tiles on every SM, but many chunks: split K over a cluster
+    // of S CTAs per row range (S <= 8, at least three chunks per part).
+    int ksplit = 1;
+    const int T0 = tmax < 7 ? tmax : 7;
+    const int nch_all = (int)(((w->k >> 7) + GEMV_PBLK - 1) / GEMV_PBLK);
+    if (ntiles < sms * (T0 - 1)) {
+        const int ng = (ntiles + T0 - 1) / T0;
+        int S = sms / ng;
+        if (S > 8) S = 8;
+        if (S > nch_all / 3) S = nch_all / 3;
+        if (S >= 2) {
+            ksplit = S;
+            ncta = ng * S;
+            T = (ntiles + ng - 1) / ng;
+        }
     }
     const uint8_t* codes = (const uint8_t*)w->data;
     const uint16_t* scales = (const uint16_t*)(codes + (size_t)w->n * (w->k / 4));
@@ -396,14 +513,14 @@ static int launch_q2_gemv_mma(const uint16_t* x, const bq_q2_weight* w, uint16_t
     if (st) return st;
     const int mm = (int)m, n = (int)w->n, k = (int)w->k, gr = (int)w->group;
     switch (T) {
-        case 1: st = launch_t<1>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
-        case 2: st = launch_t<2>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
-        case 3: st = launch_t<3>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
-        case 4: st = launch_t<4>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
-        case 5: st = launch_t<5>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
-        case 6: st = launch_t<6>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
-        case 7: st = launch_t<7>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
-        case 8: st = launch_t<8>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, stream, who); break;
+        case 1: st = launch_t<1>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, stream, who); break;
+        case 2: st = launch_t<2>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, stream, who); break;
+        case 3: st = launch_t<3>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, stream, who); break;
+        case 4: st = launch_t<4>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, stream, who); break;
+        case 5: st = launch_t<5>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, stream, who); break;
+        case 6: st = launch_t<6>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, stream, who); break;
+        case 7: st = launch_t<7>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, stream, who); break;
+        case 8: st = launch_t<8>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, stream, who); break;
         default: return fail(BQ_ERR_INVALID, "%s: internal tile count %d", who, T);
     }
     if (st) return st;

@@ -115,6 +115,20 @@ def test_gemv_small(B, m, n, k, group):
     check_bf16_vs_f64(y, ref, "gemv m=%d n=%d k=%d" % (m, n, k))
 
 
+# Shapes with few row tiles and many 1024-column chunks run as a cluster of K parts (2 CTAs
+# for (300, 8192) and (37, 6144, group 256), 3 with a partial last chunk for (40, 9856), 8 for
+# (100, 24576)); the down projection [5120, 17408] is the full-size case.
+@pytest.mark.parametrize("m", [1, 3, 8])
+@pytest.mark.parametrize("n,k,group", [(300, 8192, 128), (37, 6144, 256), (40, 9856, 128), (100, 24576, 128),
+                                       (5120, 17408, 128)])
+def test_gemv_ksplit(B, m, n, k, group):
+    d = synth.small_q2(900 + n + m, n, k, m, group=group)
+    w = dev_q2(B, d["codes"], d["scales"], group)
+    y = bf16_dev_to_u16(B.q2_gemv_batchm(to_dev_u16_as_bf16(d["x"]), w))
+    ref = O.q2_gemv(d["x"], O.q2_pack(d["codes"], d["scales"], group), n, k, group)
+    check_bf16_vs_f64(y, ref, "gemv ksplit m=%d n=%d k=%d" % (m, n, k))
+
+
 def test_gemv_closed_forms(B):
     n, k = 40, 384
     d = synth.small_q2(450, n, k, 2)
