@@ -394,7 +394,7 @@ def _rows_ffn(rows, reps, dev, hbm_peak):
                             for s in sets])
         t = _time_graph(g, reps) / len(sets)
         rows["a4_ffn_q2_m%d" % m] = {"us": t * 1e6, "weight_GBps": chain_bytes / t / 1e9,
-                                     "frac_hbm": chain_bytes / t / 1e9 / hbm_peak, "launches": 4}
+                                     "frac_hbm": chain_bytes / t / 1e9 / hbm_peak, "launches": 3}
     # per-GEMV times inside the chain at m = 8 (gate, down) and SiLU*mul alone
     xm = xf.contiguous()
     gs = torch.empty((8, inter), dtype=torch.bfloat16, device=dev)

@@ -220,6 +220,15 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// SiLU(g) * u in fp32: SiLU(z) = z * sigmoid(z), sigmoid from e = exp(-|z|) so that neither
+// branch overflows.  (The SiLU*mul kernel and the FFN chain's fused epilogue share it, so
+// both give the same bits.)
+__device__ __forceinline__ float silu_mul1(float g, float u) {
+    const float e = expf(-fabsf(g));
+    const float sig = (g >= 0.0f) ? 1.0f / (1.0f + e) : e / (1.0f + e);
+    return g * sig * u;
+}
+
 __device__ __forceinline__ uint32_t bf162_bits(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
 __device__ __forceinline__ __nv_bfloat162 bits_bf162(uint32_t u) { return *reinterpret_cast<__nv_bfloat162*>(&u); }
 

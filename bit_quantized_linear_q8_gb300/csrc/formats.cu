@@ -131,16 +131,9 @@ __global__ void __launch_bounds__(256) q8_1_kernel(const uint16_t* __restrict__ 
 }
 
 // =====================================================================================
-// SiLU(gate) * up -> BF16.  SiLU(z) = z * sigmoid(z), sigmoid from e = exp(-|z|) so that
-// neither branch overflows.
+// SiLU(gate) * up -> BF16 (silu_mul1 in common.cuh).
 // Source: dense_ffn_decode_batch.rs, `forward_km_q2` (`silu_mul`).
 // =====================================================================================
-__device__ __forceinline__ float silu_mul1(float g, float u) {
-    const float e = expf(-fabsf(g));
-    const float sig = (g >= 0.0f) ? 1.0f / (1.0f + e) : e / (1.0f + e);
-    return g * sig * u;
-}
-
 template <bool VEC>
 __global__ void __launch_bounds__(256) silu_mul_kernel(const uint16_t* __restrict__ gate, const uint16_t* __restrict__ up,
                                                        uint16_t* out, int64_t count) {

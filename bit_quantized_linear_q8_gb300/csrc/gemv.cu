@@ -177,11 +177,25 @@ __device__ __forceinline__ void gemv_issue(uint8_t* stages, int stage_bytes, uin
     gemv_issue_x<T>(stages, stage_bytes, full, xmap, c, s, m);
 }
 
+// Stores output element idx = BF16(sum).  With `hgate` (the FFN chain's up projection) it
+// also replaces hgate[idx] (the gate projection, whose value g was loaded earlier) by
+// BF16(SiLU(g) * u), u the stored BF16.
+__device__ __forceinline__ void gemv_store(uint16_t* y, uint16_t* hgate, size_t idx, float sum, uint16_t g) {
+    const __nv_bfloat16 bv = __float2bfloat16_rn(sum);
+    const uint16_t ub = *reinterpret_cast<const uint16_t*>(&bv);
+    y[idx] = ub;
+    if (hgate) {
+        const __nv_bfloat16 hb = __float2bfloat16_rn(silu_mul1(bf16_bits_to_f32(g), bf16_bits_to_f32(ub)));
+        hgate[idx] = *reinterpret_cast<const uint16_t*>(&hb);
+    }
+}
+
 template <int T>
 __global__ void __launch_bounds__(GEMV_THREADS, 1)
     q2_gemv_kernel(const __grid_constant__ CUtensorMap tmap_full, const __grid_constant__ CUtensorMap tmap_less,
                    const __grid_constant__ CUtensorMap xmap, const uint16_t* __restrict__ scales,
-                   uint16_t* __restrict__ y, int m, int n, int k, int group, int ntiles, int nstages, int ksplit) {
+                   uint16_t* __restrict__ y, int m, int n, int k, int group, int ntiles, int nstages, int ksplit,
+                   uint16_t* hgate) {
     constexpr int TQ = T;  // tiles per warp
     extern __shared__ uint8_t smem_raw[];
     uint8_t* stages = align1024(smem_raw);
@@ -278,6 +292,23 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1)
         }
     }
     __syncthreads();
+
+    // Outputs of this thread in the store loops below: o = threadIdx.x + 256 i, i < 4 (at most
+    // 8 x 128 outputs per CTA).  The fused epilogue's gate values are loaded now (the kernel
+    // before this one has finished: thread 0 waited for it before the barrier above), so
+    // their latency hides under the main loop.
+    const int per_col = nt * 16;
+    uint16_t hg[4] = {0, 0, 0, 0};
+    if (hgate) {
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int o = threadIdx.x + GEMV_THREADS * i;
+            if (o < per_col * m) {
+                const int j = o / per_col, rem = o - j * per_col;
+                if (r0 + rem < n) hg[i] = hgate[(size_t)j * n + r0 + rem];
+            }
+        }
+    }
 
     bool failed = false;
     float tot[TQ][4];
@@ -392,11 +423,13 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1)
         for (int e = 0; e < 4; e++) red[(pb * T + q) * 160 + lane * 5 + e] = tot[q][e];
     }
     __syncthreads();
-    const int per_col = nt * 16;
     float* part = red + GEMV_PBLK * T * 160;  // [m][16 T]: this CTA's sums (K parts only)
-    for (int o = threadIdx.x; o < per_col * m; o += blockDim.x) {
-        const int j = o / per_col, rem = o % per_col, tau = rem >> 4, r = rem & 15;
-        const int row = r0 + tau * 16 + r;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int o = threadIdx.x + GEMV_THREADS * i;
+        if (o >= per_col * m) break;
+        const int j = o / per_col, rem = o - j * per_col, tau = rem >> 4, r = rem & 15;
+        const int row = r0 + rem;
         if (row >= n) continue;
         const int ln = (r & 7) * 4 + (j >> 1), e = (r >> 3) * 2 + (j & 1);
         float sum = 0.f;
@@ -405,21 +438,28 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1)
         if (ksplit > 1) {
             part[j * 16 * T + rem] = sum;
         } else {
-            const __nv_bfloat16 bv = __float2bfloat16_rn(sum);
-            y[(size_t)j * n + row] = *reinterpret_cast<const uint16_t*>(&bv);
+            gemv_store(y, hgate, (size_t)j * n + row, sum, hg[i]);
         }
     }
     if (ksplit > 1) {
         cluster_sync_all();  // every member's partial sums are in its shared memory
         if (rank == 0) {
-            for (int o = threadIdx.x; o < per_col * m; o += blockDim.x) {
-                const int j = o / per_col, rem = o % per_col;
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int o = threadIdx.x + GEMV_THREADS * i;
+                if (o >= per_col * m) break;
+                const int j = o / per_col, rem = o - j * per_col;
                 const int row = r0 + rem;
                 if (row >= n) continue;
+                // all members' values requested before any is added
+                float v[8];
+#pragma unroll
+                for (int q = 1; q < 8; q++)
+                    v[q] = q < ksplit ? ld_cluster_f32(&part[j * 16 * T + rem], (uint32_t)q) : 0.f;
                 float sum = part[j * 16 * T + rem];
-                for (int q = 1; q < ksplit; q++) sum += ld_cluster_f32(&part[j * 16 * T + rem], (uint32_t)q);
-                const __nv_bfloat16 bv = __float2bfloat16_rn(sum);
-                y[(size_t)j * n + row] = *reinterpret_cast<const uint16_t*>(&bv);
+#pragma unroll
+                for (int q = 1; q < 8; q++) sum += v[q];
+                gemv_store(y, hgate, (size_t)j * n + row, sum, hg[i]);
             }
         }
         cluster_sync_all();  // members keep their shared memory until the leader has read it
@@ -428,7 +468,8 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1)
 
 template <int T>
 static int launch_t(const uint8_t* codes, const CUtensorMap& xmap, const uint16_t* scales, uint16_t* y, int m,
-                    int n, int k, int group, int ntiles, int ncta, int ksplit, cudaStream_t stream, const char* who) {
+                    int n, int k, int group, int ntiles, int ncta, int ksplit, uint16_t* hgate, cudaStream_t stream,
+                    const char* who) {
     static int configured_smem[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -468,14 +509,14 @@ static int launch_t(const uint8_t* codes, const CUtensorMap& xmap, const uint16_
     cfg.attrs = attr;
     cfg.numAttrs = ksplit > 1 ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, q2_gemv_kernel<T>, map_full, map_less, xmap, scales, y, m, n, k, group, ntiles,
-                           nstages, ksplit) != cudaSuccess)
+                           nstages, ksplit, hgate) != cudaSuccess)
         return check_launch(who);
     return BQ_OK;
 }
 
 // The warp-MMA GEMV: CTA c takes a contiguous range of T or T - 1 row tiles.
-static int launch_q2_gemv_mma(const uint16_t* x, const bq_q2_weight* w, uint16_t* y, uint32_t m,
-                              cudaStream_t stream, const char* who) {
+static int launch_q2_gemv_mma(const uint16_t* x, const bq_q2_weight* w, uint16_t* y, uint32_t m, uint16_t* hgate,
+                              bool allow_split, cudaStream_t stream, const char* who) {
     const int G = (int)(w->k / w->group);
     const int ntiles = (int)((w->n + 15) / 16);
     int tmax = GEMV_MAX_T;
@@ -494,7 +535,7 @@ static int launch_q2_gemv_mma(const uint16_t* x, const bq_q2_weight* w, uint16_t
     int ksplit = 1;
     const int T0 = tmax < 7 ? tmax : 7;
     const int nch_all = (int)(((w->k >> 7) + GEMV_PBLK - 1) / GEMV_PBLK);
-    if (ntiles < sms * (T0 - 1)) {
+    if (allow_split && ntiles < sms * (T0 - 1)) {
         const int ng = (ntiles + T0 - 1) / T0;
         int S = sms / ng;
         if (S > 8) S = 8;
@@ -513,30 +554,32 @@ static int launch_q2_gemv_mma(const uint16_t* x, const bq_q2_weight* w, uint16_t
     if (st) return st;
     const int mm = (int)m, n = (int)w->n, k = (int)w->k, gr = (int)w->group;
     switch (T) {
-        case 1: st = launch_t<1>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, stream, who); break;
-        case 2: st = launch_t<2>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, stream, who); break;
-        case 3: st = launch_t<3>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, stream, who); break;
-        case 4: st = launch_t<4>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, stream, who); break;
-        case 5: st = launch_t<5>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, stream, who); break;
-        case 6: st = launch_t<6>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, stream, who); break;
-        case 7: st = launch_t<7>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, stream, who); break;
-        case 8: st = launch_t<8>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, stream, who); break;
+        case 1: st = launch_t<1>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, hgate, stream, who); break;
+        case 2: st = launch_t<2>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, hgate, stream, who); break;
+        case 3: st = launch_t<3>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, hgate, stream, who); break;
+        case 4: st = launch_t<4>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, hgate, stream, who); break;
+        case 5: st = launch_t<5>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, hgate, stream, who); break;
+        case 6: st = launch_t<6>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, hgate, stream, who); break;
+        case 7: st = launch_t<7>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, hgate, stream, who); break;
+        case 8: st = launch_t<8>(codes, xmap, scales, y, mm, n, k, gr, ntiles, ncta, ksplit, hgate, stream, who); break;
         default: return fail(BQ_ERR_INVALID, "%s: internal tile count %d", who, T);
     }
     if (st) return st;
     return check_launch(who);
 }
 
-// Launches the GEMV for an already validated weight.
+// Launches the GEMV for an already validated weight.  With `hgate` (an [m][n] BF16 buffer
+// holding the gate projection) the epilogue also turns hgate into BF16(SiLU(hgate) * y).
+// `allow_split` permits the cluster K split.
 int launch_q2_gemv(const uint16_t* x, const bq_q2_weight* w, uint16_t* y, uint32_t m, cudaStream_t stream,
-                   const char* who) {
+                   const char* who, uint16_t* hgate = nullptr, bool allow_split = true) {
     if (m == 0 || w->n == 0) return ok();
     if (w->k == 0) {
         if (cudaMemsetAsync(y, 0, (size_t)m * w->n * 2, stream) != cudaSuccess)
             return fail(BQ_ERR_LAUNCH, "%s: memset failed", who);
         return ok();
     }
-    return launch_q2_gemv_mma(x, w, y, m, stream, who);
+    return launch_q2_gemv_mma(x, w, y, m, hgate, allow_split, stream, who);
 }
 
 static int check_gemv_args(const uint16_t* x, const bq_q2_weight* w, const uint16_t* y, uint32_t m, const char* who) {
@@ -582,11 +625,19 @@ int ffn_q2_km(const uint16_t* x, const bq_q2_weight* gate, const bq_q2_weight* u
         return fail(BQ_ERR_INVALID,
                     "%s: shapes must be gate/up [inter, hidden], down [hidden, inter] (gate %ux%u up %ux%u down %ux%u)",
                     who, gate->n, gate->k, up->n, up->k, down->n, down->k);
+    const size_t inter_bytes = (size_t)m * gate->n * 2;
+    const uintptr_t gs = reinterpret_cast<uintptr_t>(gate_scratch), us = reinterpret_cast<uintptr_t>(up_scratch);
+    if (gs < us + inter_bytes && us < gs + inter_bytes)
+        return fail(BQ_ERR_INVALID, "%s: gate_scratch and up_scratch overlap", who);
     cudaStream_t s = (cudaStream_t)stream;
     if ((st = launch_q2_gemv(x, gate, gate_scratch, m, s, who))) return st;
-    if ((st = launch_q2_gemv(x, up, up_scratch, m, s, who))) return st;
-    if ((st = silu_mul_bf16(gate_scratch, up_scratch, gate_scratch, (size_t)m * gate->n, stream))) return st;
-    return launch_q2_gemv(gate_scratch, down, out, m, s, who);
+    // the up projection's epilogue also forms h = SiLU(g) * u in gate_scratch
+    if ((st = launch_q2_gemv(x, up, up_scratch, m, s, who, gate_scratch))) return st;
+    // The down projection runs without the cluster K split here: right after the up
+    // projection a cluster launch loses its early start (measured: chain 54.9 us with the
+    // split against 48.0 us without at m = 2, equal at m = 3), while on its own the split
+    // GEMV is the faster one (13.5 against 20.8 us).
+    return launch_q2_gemv(gate_scratch, down, out, m, s, who, nullptr, false);
 }
 
 }  // extern "C"

@@ -118,7 +118,9 @@ int silu_mul_bf16(const uint16_t* gate, const uint16_t* up, uint16_t* out, size_
  *   gate_scratch = x @ gate^T; up_scratch = x @ up^T (both [m][inter] BF16);
  *   gate_scratch = SiLU(gate_scratch) * up_scratch; out = gate_scratch @ down^T ([m][hidden]).
  * Shapes: gate, up: n = inter, k = hidden; down: n = hidden, k = inter.  On return (after
- * the stream drains) gate_scratch holds h and up_scratch holds u, as on the page.
+ * the stream drains) gate_scratch holds h and up_scratch holds u, as on the page; the two
+ * must not overlap (BQ_ERR_INVALID).  Three launches: the SiLU*mul step runs in the up
+ * projection's epilogue with the same arithmetic as silu_mul_bf16.
  * Source: dense_ffn_decode_batch.rs, `forward_km_q2`. */
 int ffn_q2_km(const uint16_t* x, const bq_q2_weight* gate, const bq_q2_weight* up, const bq_q2_weight* down,
               uint16_t* gate_scratch, uint16_t* up_scratch, uint16_t* out, uint32_t m, bq_stream_t stream);
