@@ -479,7 +479,8 @@ def _rows_q4k(rows, reps, dev):
         rows["a7_q4k_ffn_prefill_m2048"] = {"us": t * 1e6, "TOPS_chain": flops / t / 1e12,
                                             "gate_gemm_us": tg * 1e6,
                                             "gate_TOPS": 2.0 * m * hidden * inter / tg / 1e12,
-                                            "pipe": "mma.sync m16n8k32 s8.u8 (legacy warp MMA)"}
+                                            "pipe": "tcgen05.mma kind::f16 M128 N256 K16: activations and Q4_K "
+                                                    "weights as hi/lo BF16 pairs (3 MMAs per K16)"}
     except Exception as e:  # reported, not hidden
         rows["a7_q4k_ffn_prefill_m2048"] = {"error": str(e)[:200]}
 

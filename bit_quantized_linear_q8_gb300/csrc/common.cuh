@@ -45,7 +45,6 @@ int make_tmap_3d_u8(CUtensorMap* map, const void* base, const uint64_t (&dims)[3
 // Reads and clears each translation unit's device status word (nonzero after a bounded
 // wait gave up).
 unsigned int gemv_status_take();
-unsigned int mmq_status_take();
 unsigned int mmq_tc_status_take();
 
 // ------------------------------------------------------------------ device helpers

@@ -190,6 +190,44 @@ __device__ __forceinline__ uint32_t u4_get(const uint4& v, int u) {
     return u == 0 ? v.x : u == 1 ? v.y : u == 2 ? v.z : v.w;
 }
 
+// Epilogue of one activation row: accumulator columns 32c .. 32c + 31 for c in [c0, c1)
+// (tensor-memory lane quadrant base tA) -> BF16 -> out[row][n0 + ...], guarding the m and n
+// tails.  All lanes of the warp call it (tcgen05.ld is warp-wide); `ok` is warp-uniform.
+__device__ __forceinline__ void qt_epilogue(uint32_t tA, int c0, int c1, int row, int m, int n, int n0, bool ok,
+                                            uint16_t* __restrict__ out) {
+    if (!ok) return;
+    const bool vec = (n & 7) == 0;
+#pragma unroll 1
+    for (int c = c0; c < c1; c++) {
+        const int col0 = n0 + 32 * c;
+        if (col0 >= n) break;  // warp-uniform
+        uint32_t v[32];
+        qt_ld32(tA + 32u * c, v);
+        if (row < m) {
+            uint16_t* dst = out + (size_t)row * n + col0;
+            if (vec && col0 + 32 <= n) {
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    uint4 o;
+                    o.x = bf162_bits(__floats2bfloat162_rn(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])));
+                    o.y = bf162_bits(__floats2bfloat162_rn(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])));
+                    o.z = bf162_bits(__floats2bfloat162_rn(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])));
+                    o.w = bf162_bits(__floats2bfloat162_rn(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+                    *reinterpret_cast<uint4*>(dst + 8 * q) = o;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; e++) {
+                    if (col0 + e < n) {
+                        const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(v[e]));
+                        dst[e] = *reinterpret_cast<const uint16_t*>(&b);
+                    }
+                }
+            }
+        }
+    }
+}
+
 // (Launch bounds of 512 threads keep ptxas at <= 128 registers: 14 warps put four warps on
 // one SM sub-partition, whose register file holds 16 K registers.)
 __global__ void __launch_bounds__(512, 1)
@@ -318,42 +356,10 @@ __global__ void __launch_bounds__(512, 1)
             mbar_arrive(&afull[st]);
         }
         // ---------------------------------------------------------------- epilogue
-        const int row = m0 + lrow;
         bool ok = mbar_wait(accfull, 0);
         ok = __all_sync(0xffffffffu, ok && !*abort) != 0;
         qt_fence_after();
-        if (ok) {
-            const bool vec = (n & 7) == 0;
-#pragma unroll 1
-            for (int c = 4 * hf; c < 4 * hf + 4; c++) {
-                const int col0 = n0 + 32 * c;
-                if (col0 >= n) break;  // warp-uniform
-                uint32_t v[32];
-                qt_ld32(tA + 32u * c, v);
-                if (row < m) {
-                    uint16_t* dst = out + (size_t)row * n + col0;
-                    if (vec && col0 + 32 <= n) {
-#pragma unroll
-                        for (int q = 0; q < 4; q++) {
-                            uint4 o;
-                            o.x = bf162_bits(__floats2bfloat162_rn(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])));
-                            o.y = bf162_bits(__floats2bfloat162_rn(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])));
-                            o.z = bf162_bits(__floats2bfloat162_rn(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])));
-                            o.w = bf162_bits(__floats2bfloat162_rn(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
-                            *reinterpret_cast<uint4*>(dst + 8 * q) = o;
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; e++) {
-                            if (col0 + e < n) {
-                                const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(v[e]));
-                                dst[e] = *reinterpret_cast<const uint16_t*>(&b);
-                            }
-                        }
-                    }
-                }
-            }
-        }
+        qt_epilogue(tA, 4 * hf, 4 * hf + 4, m0 + lrow, m, n, n0, ok, out);
     } else {
         // ---------------------------------------------------------------- weight operand
         // Thread t expands weight rows t and t + 128 of the tile.
@@ -433,14 +439,270 @@ __global__ void __launch_bounds__(512, 1)
     }
 }
 
-static int qt_reserve_smem(size_t bytes, const char* who) {
-    static int cache[64] = {0};
+// =====================================================================================
+// Q4_K.  Source: q4k_mmq.rs `q4k_mmq_gemm` (C[m, n] = A[m, k] x W[n, k], BF16 store) with
+// block_q4_K weights w = d sc_j q - dmin m_j (256 values, 144 bytes: fp16 d, fp16 dmin, 12
+// bytes of 6-bit sc_j / m_j, 128 bytes of 4-bit codes; byte 32c + l holds value l of
+// sub-block 2c in its low nibble and of sub-block 2c + 1 in its high nibble).
+//
+// The weight w (fp32: d sc_j q is exact, the difference rounds once) is not exact in BF16,
+// so it is split like the activations: wh = bf16(w), wl = bf16(w - wh).  Three MMAs per
+// K16 slice, A_hi B_hi + A_lo B_hi + A_hi B_lo, into one fp32 accumulator; the dropped
+// A_lo B_lo term is below 2^-17 of each product.  The dmin m_j term is inside the operand.
+//  * Tile 128 (m) x 256 (n), K step 64 (a quarter super-block: sub-blocks 2t, 2t + 1 whose
+//    codes are the 32 bytes 16 + 32t of the block).  Natural K order within a step.
+//  * Tensor memory: accumulator (256 columns) + four activation stages (hi, lo: 64 columns).
+//    Shared memory: two weight stages (hi and lo halves, 2 x 32 KB) + a three-step TMA ring
+//    (q8_1 codes, (d, s) pairs, the weight codes and the 16-byte block headers).
+//  * Warp 0 issues the MMAs; warps 1-4 expand activations (one row per thread) and run the
+//    epilogue; warps 5-12 expand weights (one row per thread); warp 13 is the TMA producer.
+// =====================================================================================
+constexpr int Q4T_NSA = 4;                       // activation stages (tensor memory)
+constexpr int Q4T_NSB = 2;                       // weight stages (shared memory)
+constexpr int Q4T_NR = 3;                        // ring stages
+constexpr int Q4T_AWARP0 = 1, Q4T_BWARP0 = 5, Q4T_PWARP = 13;
+constexpr int Q4T_THREADS = 14 * 32;
+constexpr uint32_t Q4T_BHALF = QT_BN * 64 * 2;   // 32 KB: the hi or the lo half of a stage
+constexpr uint32_t Q4T_BSTAGE = 2 * Q4T_BHALF;
+constexpr uint32_t Q4T_R_A = 0;                  // q8_1 codes [4 runs][128 rows][16 B]
+constexpr uint32_t Q4T_R_D = 8192;               // (d, s) pairs [128 rows][16 B]
+constexpr uint32_t Q4T_R_Q = 10240;              // weight codes [2][256 rows][16 B]
+constexpr uint32_t Q4T_R_H = 18432;              // block headers [256 rows][16 B]
+constexpr uint32_t Q4T_RSTAGE = 22528;
+static_assert(QT_ACOL + 64 * Q4T_NSA <= QT_TMEM_COLS, "tensor memory budget");
+static_assert(Q4T_BWARP0 == Q4T_AWARP0 + 4 && Q4T_PWARP == Q4T_BWARP0 + QT_BN / 32 && Q4T_THREADS == (Q4T_PWARP + 1) * 32,
+              "warp roles");
+constexpr size_t Q4T_SMEM = 1024 + (size_t)Q4T_NSB * Q4T_BSTAGE + (size_t)Q4T_NR * Q4T_RSTAGE +
+                            (2 * Q4T_NSA + 2 * Q4T_NSB + 2 * Q4T_NR + 1) * 8 + 16;
+static_assert(Q4T_SMEM <= 227 * 1024, "shared memory budget");
+
+// Byte i (0..11) of the 12 scale bytes held in the words a, b, c.
+__device__ __forceinline__ int q4t_sbyte(uint32_t a, uint32_t b, uint32_t c, int i) {
+    const uint32_t w = i < 4 ? a : (i < 8 ? b : c);
+    return (int)((w >> (8 * (i & 3))) & 0xFFu);
+}
+
+// 6-bit scale and min of sub-block j from the 12 scale bytes (the block_q4_K packing).
+__device__ __forceinline__ void q4t_scale_min(uint32_t a, uint32_t b, uint32_t c, int j, int& sc, int& mn) {
+    if (j < 4) {
+        sc = q4t_sbyte(a, b, c, j) & 63;
+        mn = q4t_sbyte(a, b, c, j + 4) & 63;
+    } else {
+        sc = (q4t_sbyte(a, b, c, j + 4) & 15) | ((q4t_sbyte(a, b, c, j - 4) >> 6) << 4);
+        mn = (q4t_sbyte(a, b, c, j + 4) >> 4) | ((q4t_sbyte(a, b, c, j) >> 6) << 4);
+    }
+}
+
+// Two 4-bit codes (bytes b0, b0 + 1 of nib, each 0..15) -> w = q D - M (fp32), split into
+// a BF16 pair hi and a BF16 pair lo.
+__device__ __forceinline__ void q4t_split_pair(uint32_t nib, uint32_t sel0, uint32_t sel1, float D, float M,
+                                               uint32_t& hi, uint32_t& lo) {
+    const float f0 = __uint_as_float(__byte_perm(nib, 0x4B000000u, sel0));  // 2^23 + q
+    const float f1 = __uint_as_float(__byte_perm(nib, 0x4B000000u, sel1));
+    const float2 q = __fadd2_rn(make_float2(f0, f1), make_float2(-8388608.0f, -8388608.0f));
+    const float2 w = __ffma2_rn(q, make_float2(D, D), make_float2(-M, -M));
+    hi = bf162_bits(__floats2bfloat162_rn(w.x, w.y));
+    const float2 h = make_float2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xFFFF0000u));
+    const float2 r = __fadd2_rn(w, make_float2(-h.x, -h.y));
+    lo = bf162_bits(__floats2bfloat162_rn(r.x, r.y));
+}
+
+__global__ void __launch_bounds__(512, 1)
+    q4k_mmq_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapD,
+                      const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapH,
+                      uint16_t* __restrict__ out, int m, int n, int k, int ntn) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* bst = align1024(smem_raw);
+    uint8_t* ring = bst + Q4T_NSB * Q4T_BSTAGE;
+    uint64_t* afull = reinterpret_cast<uint64_t*>(ring + Q4T_NR * Q4T_RSTAGE);
+    uint64_t* aempty = afull + Q4T_NSA;
+    uint64_t* bfull = aempty + Q4T_NSA;
+    uint64_t* bempty = bfull + Q4T_NSB;
+    uint64_t* rfull = bempty + Q4T_NSB;
+    uint64_t* rempty = rfull + Q4T_NR;
+    uint64_t* accfull = rempty + Q4T_NR;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(accfull + 1);
+    volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int n0 = (blockIdx.x % ntn) * QT_BN, m0 = (blockIdx.x / ntn) * QT_BM;
+    const int S = k >> 6;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < Q4T_NSA; s++) {
+            mbar_init(&afull[s], 4 * 32);
+            mbar_init(&aempty[s], 1);
+        }
+        for (int s = 0; s < Q4T_NSB; s++) {
+            mbar_init(&bfull[s], 8 * 32);
+            mbar_init(&bempty[s], 1);
+        }
+        for (int r = 0; r < Q4T_NR; r++) {
+            mbar_init(&rfull[r], 1);
+            mbar_init(&rempty[r], 12);  // one arrival per consuming warp
+        }
+        mbar_init(accfull, 1);
+        *abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                     "n"(QT_TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    qt_fence_before();
+    __syncthreads();
+    qt_fence_after();
+    const uint32_t tbase = *tslot;
+
+    if (warp == Q4T_PWARP) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            for (int s = 0; s < S; s++) {
+                const int r = s % Q4T_NR;
+                if (s >= Q4T_NR && !qt_wait(&rempty[r], (uint32_t)((s / Q4T_NR) - 1) & 1u, abort)) break;
+                const int sb = s >> 2, t = s & 3;
+                uint8_t* dst = ring + r * Q4T_RSTAGE;
+                mbar_arrive_expect_tx(&rfull[r], Q4T_RSTAGE);
+                tma_load_3d(dst + Q4T_R_A, &mapA, 0, m0, 4 * s, &rfull[r]);
+                tma_load_2d(dst + Q4T_R_D, &mapD, 16 * s, m0, &rfull[r]);
+                tma_load_3d(dst + Q4T_R_Q, &mapQ, 0, n0, 9 * sb + 1 + 2 * t, &rfull[r]);
+                tma_load_3d(dst + Q4T_R_H, &mapH, 0, n0, 9 * sb, &rfull[r]);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 0) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            for (int s = 0; s < S; s++) {
+                const int sa = s % Q4T_NSA, sbi = s % Q4T_NSB;
+                if (!qt_wait(&afull[sa], (uint32_t)(s / Q4T_NSA) & 1u, abort) ||
+                    !qt_wait(&bfull[sbi], (uint32_t)(s / Q4T_NSB) & 1u, abort))
+                    break;
+                qt_fence_after();
+                const uint32_t bhi = smem_u32(bst + sbi * Q4T_BSTAGE), blo = bhi + Q4T_BHALF;
+                const uint32_t abase = tbase + QT_ACOL + 64u * sa;
+#pragma unroll
+                for (int kk = 0; kk < 4; kk++) {
+                    const uint64_t dh = qt_smem_desc(bhi + 256u * kk, 128u, 1024u);
+                    const uint64_t dl = qt_smem_desc(blo + 256u * kk, 128u, 1024u);
+                    qt_mma(tbase, abase + 8u * kk, dh, (s | kk) != 0);   // A_hi B_hi
+                    qt_mma(tbase, abase + 32u + 8u * kk, dh, 1u);        // A_lo B_hi
+                    qt_mma(tbase, abase + 8u * kk, dl, 1u);              // A_hi B_lo
+                }
+                qt_commit(&aempty[sa]);
+                qt_commit(&bempty[sbi]);
+            }
+            qt_commit(accfull);  // completes once every MMA issued above has finished
+            if (!mbar_wait(accfull, 0)) atomicOr(&g_mmq_tc_status, 2u);
+        }
+        __syncwarp();
+    } else if (warp < Q4T_BWARP0) {
+        // ---------------------------------------------------------------- activation operand
+        const int qd = warp & 3;
+        const int lrow = 32 * qd + lane;
+        const uint32_t tA = tbase + ((uint32_t)(32 * qd) << 16);
+        for (int s = 0; s < S; s++) {
+            const int sa = s % Q4T_NSA, r = s % Q4T_NR;
+            if (!qt_wait_warp(&rfull[r], (uint32_t)(s / Q4T_NR) & 1u, abort)) break;
+            const uint8_t* rs = ring + r * Q4T_RSTAGE;
+            uint4 cr[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) cr[i] = *reinterpret_cast<const uint4*>(rs + Q4T_R_A + i * 2048 + lrow * 16);
+            const float4 dp = *reinterpret_cast<const float4*>(rs + Q4T_R_D + lrow * 16);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&rempty[r]);
+            if (s >= Q4T_NSA) {
+                if (!qt_wait_warp(&aempty[sa], (uint32_t)((s / Q4T_NSA) - 1) & 1u, abort)) break;
+                qt_fence_after();
+            }
+            const uint32_t tcol = tA + QT_ACOL + 64u * sa;
+#pragma unroll
+            for (int i = 0; i < 4; i++) {  // run i: columns 16i .. 16i + 15, q8_1 block i / 2
+                const float d = i < 2 ? dp.x : dp.z;
+                uint32_t hw[8], lw[8];
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    const uint32_t wb = u4_get(cr[i], u) ^ 0x80808080u;
+                    // words 8i + 2u + p: columns 16i + 4u + 2p, + 1
+                    qt_split_pair(wb, 0x7540u, 0x7541u, d, hw[2 * u], lw[2 * u]);
+                    qt_split_pair(wb, 0x7542u, 0x7543u, d, hw[2 * u + 1], lw[2 * u + 1]);
+                }
+                qt_st8(tcol + 8u * i, hw);
+                qt_st8(tcol + 32u + 8u * i, lw);
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            qt_fence_before();
+            mbar_arrive(&afull[sa]);
+        }
+        bool ok = mbar_wait(accfull, 0);
+        ok = __all_sync(0xffffffffu, ok && !*abort) != 0;
+        qt_fence_after();
+        qt_epilogue(tA, 0, QT_BN / 32, m0 + lrow, m, n, n0, ok, out);
+    } else {
+        // ---------------------------------------------------------------- weight operand
+        const int bt = 32 * (warp - Q4T_BWARP0) + lane;  // weight row within the tile
+        for (int s = 0; s < S; s++) {
+            const int sbi = s % Q4T_NSB, r = s % Q4T_NR, t = s & 3;
+            if (!qt_wait_warp(&rfull[r], (uint32_t)(s / Q4T_NR) & 1u, abort)) break;
+            const uint8_t* rs = ring + r * Q4T_RSTAGE;
+            const uint4 hdr = *reinterpret_cast<const uint4*>(rs + Q4T_R_H + bt * 16);
+            const uint4 q0 = *reinterpret_cast<const uint4*>(rs + Q4T_R_Q + bt * 16);
+            const uint4 q1 = *reinterpret_cast<const uint4*>(rs + Q4T_R_Q + 4096 + bt * 16);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&rempty[r]);
+            // D_j = d sc_j, M_j = dmin m_j of sub-blocks 2t (low nibbles) and 2t + 1 (high)
+            const float dd = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xFFFFu)));
+            const float dm = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
+            int sc0, mn0, sc1, mn1;
+            q4t_scale_min(hdr.y, hdr.z, hdr.w, 2 * t, sc0, mn0);
+            q4t_scale_min(hdr.y, hdr.z, hdr.w, 2 * t + 1, sc1, mn1);
+            const float D0 = dd * (float)sc0, M0 = dm * (float)mn0;
+            const float D1 = dd * (float)sc1, M1 = dm * (float)mn1;
+            if (s >= Q4T_NSB) {
+                if (!qt_wait_warp(&bempty[sbi], (uint32_t)((s / Q4T_NSB) - 1) & 1u, abort)) break;
+            }
+            uint8_t* dsth = bst + sbi * Q4T_BSTAGE + (bt >> 3) * 1024 + (bt & 7) * 16;
+            uint8_t* dstl = dsth + Q4T_BHALF;
+#pragma unroll
+            for (int v = 0; v < 4; v++) {  // code bytes 8v .. 8v + 7: columns 8v .. (low), 32 + 8v .. (high)
+                const uint32_t w0 = u4_get(v < 2 ? q0 : q1, (2 * v) & 3);
+                const uint32_t w1 = u4_get(v < 2 ? q0 : q1, (2 * v + 1) & 3);
+                uint32_t hl[4], ll[4], hh[4], lh[4];
+#pragma unroll
+                for (int e = 0; e < 2; e++) {
+                    const uint32_t w = e ? w1 : w0;
+                    const uint32_t nl = w & 0x0F0F0F0Fu, nh = (w >> 4) & 0x0F0F0F0Fu;
+                    q4t_split_pair(nl, 0x7540u, 0x7541u, D0, M0, hl[2 * e], ll[2 * e]);
+                    q4t_split_pair(nl, 0x7542u, 0x7543u, D0, M0, hl[2 * e + 1], ll[2 * e + 1]);
+                    q4t_split_pair(nh, 0x7540u, 0x7541u, D1, M1, hh[2 * e], lh[2 * e]);
+                    q4t_split_pair(nh, 0x7542u, 0x7543u, D1, M1, hh[2 * e + 1], lh[2 * e + 1]);
+                }
+                // words 4v .. 4v + 3 (core matrix v) and 16 + 4v .. (core matrix 4 + v)
+                *reinterpret_cast<uint4*>(dsth + v * 128) = make_uint4(hl[0], hl[1], hl[2], hl[3]);
+                *reinterpret_cast<uint4*>(dstl + v * 128) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+                *reinterpret_cast<uint4*>(dsth + (4 + v) * 128) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+                *reinterpret_cast<uint4*>(dstl + (4 + v) * 128) = make_uint4(lh[0], lh[1], lh[2], lh[3]);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(&bfull[sbi]);
+        }
+    }
+
+    qt_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        qt_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "n"(QT_TMEM_COLS));
+    }
+}
+
+static int qt_reserve_smem(const void* fn, int* cache, size_t bytes, const char* who) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 64) dev = 63;
     if ((size_t)cache[dev] < bytes) {
-        if (cudaFuncSetAttribute((const void*)q2_mmq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)bytes) != cudaSuccess)
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
             return fail(BQ_ERR_LAUNCH, "%s: cannot reserve %zu bytes of shared memory", who, bytes);
         cache[dev] = (int)bytes;
     }
@@ -480,11 +742,49 @@ extern "C" int q2_mmq_gemm(const void* act_q8, const bq_q2_weight* w, uint16_t* 
     if ((st = make_tmap_3d_u8(&mD, ds, {16, m, kp / 64}, {kp / 4, 16}, {16, QT_BM, 2}, who))) return st;
     // weight codes [n rows][k/4 B]: box {16 B, 256 rows}
     if ((st = make_tmap_2d_u8(&mB, wcodes, k / 4, n, k / 4, 16, QT_BN, false, who))) return st;
-    if ((st = qt_reserve_smem(QT_SMEM, who))) return st;
+    static int cache[64] = {0};
+    if ((st = qt_reserve_smem((const void*)q2_mmq_tc_kernel, cache, QT_SMEM, who))) return st;
     const int ntn = (int)((n + QT_BN - 1) / QT_BN);
     const uint64_t tiles = (uint64_t)ntn * ((m + QT_BM - 1) / QT_BM);
     if (tiles > 0x7FFFFFFFull) return fail(BQ_ERR_INVALID, "%s: shape too large", who);
     q2_mmq_tc_kernel<<<(unsigned)tiles, QT_THREADS, QT_SMEM, (cudaStream_t)stream>>>(mA, mD, mB, wsc, out, (int)m,
                                                                                    (int)n, (int)k, ntn);
+    return check_launch(who);
+}
+
+extern "C" int q4k_mmq_gemm(const void* act_q8, const void* w_q4k, uint16_t* out, uint32_t m, uint32_t n, uint32_t k,
+                            bq_stream_t stream) {
+    const char* who = "q4k_mmq_gemm";
+    if (k % 256 != 0) return fail(BQ_ERR_INVALID, "%s: k = %u must be a multiple of 256", who, k);
+    if (m == 0 || n == 0) return ok();
+    if (!out || !aligned16(out)) return fail(BQ_ERR_INVALID, "%s: out NULL or not 16-byte aligned", who);
+    if (k == 0) {
+        if (cudaMemsetAsync(out, 0, (size_t)m * n * 2, (cudaStream_t)stream) != cudaSuccess)
+            return fail(BQ_ERR_LAUNCH, "%s: memset failed", who);
+        return ok();
+    }
+    if (!act_q8 || !aligned16(act_q8) || !w_q4k || !aligned16(w_q4k))
+        return fail(BQ_ERR_INVALID, "%s: act_q8 / w_q4k NULL or not 16-byte aligned", who);
+    if (m > (1u << 24) || n > (1u << 24) || k > (1u << 24)) return fail(BQ_ERR_INVALID, "%s: shape too large", who);
+    const uint64_t kp = k;  // k % 256 == 0: no padding
+    const uint8_t* codes = (const uint8_t*)act_q8;
+    const uint8_t* ds = codes + (uint64_t)m * kp;
+    const uint64_t wrow = (uint64_t)(k / 256) * 144;  // bytes per weight row, a multiple of 16
+    int st;
+    CUtensorMap mA, mD, mQ, mH;
+    // q8_1 codes as [kp/16 runs][m rows][16 B]: box {16 B, 128 rows, 4 runs}
+    if ((st = make_tmap_3d_u8(&mA, codes, {16, m, kp / 16}, {kp, 16}, {16, QT_BM, 4}, who))) return st;
+    // (d, s) pairs [m rows][kp/4 B]: box {16 B (two pairs), 128 rows}
+    if ((st = make_tmap_2d_u8(&mD, ds, kp / 4, m, kp / 4, 16, QT_BM, false, who))) return st;
+    // weight blocks as [wrow/16 pieces][n rows][16 B]: codes box {16, 256, 2}, header box {16, 256, 1}
+    if ((st = make_tmap_3d_u8(&mQ, w_q4k, {16, n, wrow / 16}, {wrow, 16}, {16, QT_BN, 2}, who))) return st;
+    if ((st = make_tmap_3d_u8(&mH, w_q4k, {16, n, wrow / 16}, {wrow, 16}, {16, QT_BN, 1}, who))) return st;
+    static int cache[64] = {0};
+    if ((st = qt_reserve_smem((const void*)q4k_mmq_tc_kernel, cache, Q4T_SMEM, who))) return st;
+    const int ntn = (int)((n + QT_BN - 1) / QT_BN);
+    const uint64_t tiles = (uint64_t)ntn * ((m + QT_BM - 1) / QT_BM);
+    if (tiles > 0x7FFFFFFFull) return fail(BQ_ERR_INVALID, "%s: shape too large", who);
+    q4k_mmq_tc_kernel<<<(unsigned)tiles, Q4T_THREADS, Q4T_SMEM, (cudaStream_t)stream>>>(mA, mD, mQ, mH, out, (int)m,
+                                                                                      (int)n, (int)k, ntn);
     return check_launch(who);
 }

@@ -156,7 +156,11 @@ int ffn_q2_km_noalloc(const uint16_t* x, const bq_q2_weight* gate, const bq_q2_w
  * Source: init_q2.rs, `qkvz_q2_prefill_gemm` (MMQ route, `q2_0_mmq_gemm`). */
 int q2_mmq_gemm(const void* act_q8, const bq_q2_weight* w, uint16_t* out, uint32_t m, bq_stream_t stream);
 
-/* Q4_K MMQ: out[m][n] = q8_1(act) @ W_q4k^T, BF16 store.  k % 256 == 0.
+/* Q4_K MMQ: out[m][n] = q8_1(act) @ W_q4k^T, i.e. sum_k (d_a q)[m][k] * w[n][k] with
+ * w = d sc_j q - dmin m_j, fp32 accumulation, BF16 store.  k % 256 == 0.  Computed on the
+ * BF16 tensor cores: each activation value and each weight enters as a pair of BF16 values
+ * whose sum equals it to 2^-17 relative (three products per pair of pairs; the product of
+ * the two small halves is dropped).
  * Source: q4k_mmq.rs, `q4k_mmq_gemm` (C[m, n] = A[m, k] x W[n, k], BF16 store). */
 int q4k_mmq_gemm(const void* act_q8, const void* w_q4k, uint16_t* out, uint32_t m, uint32_t n, uint32_t k,
                  bq_stream_t stream);
