@@ -81,6 +81,20 @@ def test_status_codes_without_launch(L):
     d = W(0x1000, 256, 384, 128)
     p = ctypes.c_void_p(0x4000)
     assert L.ffn_q2_km(p, ctypes.byref(g), ctypes.byref(u), ctypes.byref(d), p, p, p, 2, null) == 1
+    # FFN scratch buffers that overlap: the up projection's epilogue reads the gate buffer
+    # while it writes the up buffer, so they must be disjoint ([2][512] BF16 = 2048 bytes each)
+    d = W(0x1000, 256, 512, 128)
+    gs, us, out = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x10000 + 1024), ctypes.c_void_p(0x20000)
+    assert L.ffn_q2_km(p, ctypes.byref(g), ctypes.byref(u), ctypes.byref(d), gs, us, out, 2, null) == 1
+    assert b"overlap" in L.bq_last_error()
+    assert L.ffn_q2_km(p, ctypes.byref(g), ctypes.byref(u), ctypes.byref(d), gs, gs, out, 2, null) == 1
+    # MMQ argument checks: Q2 needs group 128, Q4_K needs k % 256 == 0
+    w256 = W(0x1000, 64, 512, 256)
+    assert L.q2_mmq_gemm(ctypes.c_void_p(0x2000), ctypes.byref(w256), ctypes.c_void_p(0x3000), 4, null) == 1
+    assert b"group size 128" in L.bq_last_error()
+    assert L.q4k_mmq_gemm(ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000), ctypes.c_void_p(0x4000), 4, 8, 300,
+                          null) == 1
+    assert b"multiple of 256" in L.bq_last_error()
 
 
 def test_python_binding_refuses_cpu_tensors(L):
