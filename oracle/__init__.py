@@ -61,6 +61,9 @@ def lib():
             "orc_quantize_q4k": (None, [P, I, I, P]),
             "orc_dequant_q4k": (None, [P, I, I, P]),
             "orc_q4k_mmq": (None, [P, P, I, I, I, P, I, P]),
+            "orc_e2m1_value": (ctypes.c_double, [ctypes.c_int]),
+            "orc_e4m3_value": (ctypes.c_double, [ctypes.c_int]),
+            "orc_dequant_nvfp4": (None, [P, P, ctypes.c_float, I, I, P]),
             "orc_num_threads": (ctypes.c_int, []),
         }
         for name, (res, args) in sig.items():
@@ -247,4 +250,24 @@ def q4k_mmq(act, blocks, m: int, n: int, k: int, rows=None):
     rows = np.arange(m, dtype=np.int64) if rows is None else _c(rows, np.int64)
     out = np.zeros((rows.size, n), dtype=np.float64)
     lib().orc_q4k_mmq(_p(act), _p(blocks), m, n, k, _p(rows), rows.size, _p(out))
+    return out
+
+
+def e2m1_value(code: int) -> float:
+    """FP4 E2M1 code (0..15) -> its real value (OCP microscaling formats)."""
+    return lib().orc_e2m1_value(int(code))
+
+
+def e4m3_value(b: int) -> float:
+    """FP8 E4M3 byte -> its real value (OCP 8-bit floating point; 0x7F / 0xFF are NaN)."""
+    return lib().orc_e4m3_value(int(b))
+
+
+def dequant_nvfp4(packed, scales, scale2: float, n: int, k: int):
+    """NVFP4 [n, k] (packed E2M1 [n][k/2], E4M3 scales [n][k/16], fp32 scale2) -> BF16 bits,
+    the exact product rounded once (q4k_mmq.rs, `dequant_nvfp4_to_bf16`)."""
+    packed = _c(packed, np.uint8)
+    scales = _c(scales, np.uint8)
+    out = np.zeros((n, k), dtype=np.uint16)
+    lib().orc_dequant_nvfp4(_p(packed), _p(scales), ctypes.c_float(scale2), n, k, _p(out))
     return out

@@ -434,6 +434,46 @@ void orc_q4k_mmq(const uint8_t* act, const uint8_t* w, int64_t m, int64_t n, int
     }
 }
 
+/* ------------------------------------------------------------------------------ */
+/* NVFP4 weights (q4k_mmq.rs, `dequant_nvfp4_to_bf16`: "packed E2M1, E4M3 group      */
+/* scales and the per-tensor scale2" -> BF16 [n, k], one block per row).  The page    */
+/* prints the launch contract only; the readings taken here:                          */
+/*  - packed [n][k/2] bytes: value 2j of a row in the low nibble of byte j, value     */
+/*    2j + 1 in the high nibble;                                                      */
+/*  - scales [n][k/16] E4M3 bytes, one per 16 consecutive values of a row;            */
+/*  - w = e2m1(code) * e4m3(scale) * scale2, the exact real product rounded once to    */
+/*    BF16 (round to nearest even).                                                   */
+/* ------------------------------------------------------------------------------ */
+
+/* FP4 E2M1 (OCP microscaling formats): bit 3 sign, bits 1-2 exponent (bias 1), bit 0 */
+/* mantissa; exponent 0 is subnormal (0 or 0.5).  Magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6. */
+double orc_e2m1_value(int code) {
+    int s = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+    double v = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -v : v;
+}
+
+/* FP8 E4M3 (OCP 8-bit floating point): bit 7 sign, bits 3-6 exponent (bias 7), bits  */
+/* 0-2 mantissa; exponent 0 is subnormal (m * 2^-9); exponent 15 with mantissa 7 is  */
+/* NaN and there are no infinities, so the largest value is 448.                      */
+double orc_e4m3_value(int b) {
+    int s = (b >> 7) & 1, e = (b >> 3) & 15, m = b & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = (e == 0) ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+void orc_dequant_nvfp4(const uint8_t* packed, const uint8_t* scales, float scale2, int64_t n, int64_t k,
+                       uint16_t* out) {
+    for (int64_t r = 0; r < n; r++)
+        for (int64_t c = 0; c < k; c++) {
+            uint8_t byte = packed[r * (k / 2) + c / 2];
+            int code = (c % 2 == 0) ? (byte & 15) : (byte >> 4);
+            double w = orc_e2m1_value(code) * orc_e4m3_value(scales[r * (k / 16) + c / 16]) * (double)scale2;
+            out[r * k + c] = orc_f64_to_bf16(w); /* the product has <= 30 bits: exact in fp64 */
+        }
+}
+
 int orc_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -389,3 +389,46 @@ def test_q4k_mmq_matches_numpy():
     blk = _hand_block(0x3C00, 0x3400, np.ones(8, int), np.arange(8), np.zeros(256, int))
     w = O.dequant_q4k(blk, 1, 256)[0]
     assert np.array_equal(w, -0.25 * (np.arange(256) // 32))
+
+
+# ------------------------------------------------------------------------------ NVFP4
+# The page (q4k_mmq.rs, `dequant_nvfp4_to_bf16`) names packed E2M1 values, E4M3 group scales
+# and a per-tensor scale2; the values of the two element formats are fixed by the OCP
+# microscaling (FP4 E2M1) and OCP 8-bit floating point (E4M3) specifications.
+def test_e2m1_values_are_the_published_table():
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert [O.e2m1_value(c) for c in range(8)] == mags
+    assert [O.e2m1_value(8 + c) for c in range(8)] == [-v for v in mags]
+    assert np.signbit(O.e2m1_value(8))  # code 8 is -0
+
+
+def test_e4m3_endpoints_and_order():
+    assert O.e4m3_value(0x38) == 1.0
+    assert O.e4m3_value(0x7E) == 448.0          # largest finite value (no infinities)
+    assert O.e4m3_value(0x08) == 2.0 ** -6      # smallest normal
+    assert O.e4m3_value(0x01) == 2.0 ** -9      # smallest subnormal
+    assert O.e4m3_value(0x00) == 0.0
+    assert np.isnan(O.e4m3_value(0x7F)) and np.isnan(O.e4m3_value(0xFF))
+    pos = [O.e4m3_value(b) for b in range(0x7F)]  # 0x00 .. 0x7E
+    assert all(a < b for a, b in zip(pos, pos[1:]))  # strictly increasing with the byte
+    assert [O.e4m3_value(0x80 | b) for b in range(1, 0x7F)] == [-v for v in pos[1:]]
+
+
+def test_nvfp4_dequant_worked_examples():
+    import torch
+    # one row of 32 values: codes 0..15 twice (low nibble first), scales 2.0 (0x40) and
+    # 1.875 (0x3F); scale2 = 1 + 2^-10, so every product has <= 17 significant bits and is
+    # exact in fp32: torch's own fp32 -> BF16 rounding then gives the expected bits
+    codes = np.concatenate([np.arange(16), np.arange(16)]).astype(np.uint8)
+    packed = (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8).reshape(1, 16)
+    scales = np.array([[0x40, 0x3F]], np.uint8)
+    s2 = np.float32(1 + 2.0 ** -10)
+    mags = np.array([0, .5, 1, 1.5, 2, 3, 4, 6], np.float64)
+    e2m1 = np.concatenate([mags, -mags])
+    want = np.concatenate([e2m1 * 2.0, e2m1 * 1.875]) * float(s2)
+    ref = torch.tensor(want.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    out = O.dequant_nvfp4(packed, scales, float(s2), 1, 32)[0]
+    assert np.array_equal(out, ref)
+    # exact BF16 values survive unchanged; code 8 with any scale is -0
+    out = O.dequant_nvfp4(packed, np.array([[0x38, 0x38]], np.uint8), 1.0, 1, 32)[0]
+    assert out[8] == 0x8000 and out[1] == 0x3F00 and out[7] == 0x40C0  # -0, 0.5, 6.0
