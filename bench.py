@@ -350,7 +350,28 @@ def measure_rows(args, dev, hbm_peak, bf16_peak):
         _rows_prefill(rows, reps, dev, hbm_peak, bf16_peak)
     if "q4k" in groups:
         _rows_q4k(rows, reps, dev)
+    if "nvfp4" in groups:
+        _rows_nvfp4(rows, reps, dev, hbm_peak)
     return rows
+
+
+def _rows_nvfp4(rows, reps, dev, hbm_peak):
+    import torch
+    import bit_quantized_linear_q8_gb300 as B
+    from bit_quantized_linear_q8_gb300 import synth
+
+    # NVFP4 -> BF16 dequantisation of the FFN gate weight [17408, 5120] (the step before the
+    # Q4_K quantiser): reads k/2 + k/16 bytes per row, writes 2k
+    d = synth.nvfp4_ffn_weight()
+    n, k = d["n"], d["k"]
+    packed = torch.from_numpy(d["packed"]).to(dev)
+    scales = torch.from_numpy(d["scales"]).to(dev)
+    out = torch.empty((n, k), dtype=torch.bfloat16, device=dev)
+    t = _time_calls(lambda i: B.dequant_nvfp4_to_bf16(packed, scales, d["scale2"], n, k, out=out), reps)
+    nb = n * (k // 2) + n * (k // 16) + n * k * 2
+    rows["a10_nvfp4_dequant_17408x5120"] = {"us": t * 1e6, "GBps": nb / t / 1e9, "frac_hbm": nb / t / 1e9 / hbm_peak}
+    del packed, scales, out
+    torch.cuda.empty_cache()
 
 
 def _rows_gemv1024(rows, reps, dev, hbm_peak):
@@ -548,8 +569,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=16, help="distinct qkvz layer weights per step")
     ap.add_argument("--no-rows", action="store_true", help="headline only")
-    ap.add_argument("--rows", default="gemv1024,ffn,prefill,q4k",
-                    help="row groups to measure: gemv1024 (a1), ffn (a2-a4), prefill (a5, a6, a8, a9), q4k (a7)")
+    ap.add_argument("--rows", default="gemv1024,ffn,prefill,q4k,nvfp4",
+                    help="row groups to measure: gemv1024 (a1), ffn (a2-a4), prefill (a5, a6, a8, a9), q4k (a7), "
+                         "nvfp4 (NVFP4 -> BF16 weight preparation)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)

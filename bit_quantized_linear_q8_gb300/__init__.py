@@ -203,6 +203,21 @@ def dequant_q2_to_bf16(w: Q2Weight, out=None):
     return out
 
 
+def dequant_nvfp4_to_bf16(packed, scales, scale2: float, n: int, k: int, out=None):
+    """NVFP4 [n, k] -> BF16 [n, k]: packed E2M1 codes [n, k/2] (uint8), E4M3 scale bytes
+    [n, k/16] (uint8) and the per-tensor fp32 scale2 (q4k_mmq.rs, `dequant_nvfp4_to_bf16`)."""
+    torch = _torch()
+    _need(packed, torch.uint8, "packed")
+    _need(scales, torch.uint8, "scales")
+    if packed.numel() != n * (k // 2) or scales.numel() != n * (k // 16):
+        raise ValueError("packed must hold n*k/2 bytes and scales n*k/16 bytes")
+    if out is None:
+        out = torch.empty((n, k), dtype=torch.bfloat16, device=packed.device)
+    check(lib().dequant_nvfp4_to_bf16(_ptr(packed), _ptr(scales), _ptr(out), ctypes.c_float(scale2), n, k,
+                                      _stream()))
+    return out
+
+
 def q2_prefill_proj(x, w: Q2Weight, mode: str = "mmq", act_q8=None, scratch=None):
     """The prefill projection out = x @ W^T by either route of init_q2.rs
     `qkvz_q2_prefill_gemm`: "mmq" (q8_1 quantisation + Q2 MMQ, group 128 only) or

@@ -131,6 +131,83 @@ __global__ void __launch_bounds__(256) q8_1_kernel(const uint16_t* __restrict__ 
 }
 
 // =====================================================================================
+// NVFP4 -> BF16: w = e2m1(code) * e4m3(scale) * scale2, the exact product rounded once to
+// BF16.  Layout: codes [n][k/2] bytes (value 2j in the low nibble of byte j), one E4M3
+// scale byte per 16 values [n][k/16].  One CTA per row, 256 threads (the page's launch).
+// e2m1 * e4m3 is exact in fp32; the product with scale2 is taken with round-to-odd in
+// fp32 (truncate, then set the last bit if the FMA residual is nonzero), and rounding
+// that to BF16 to nearest equals rounding the exact product once, because fp32 carries
+// more than two extra bits (Boldo and Melquiond, "When double rounding is odd", 2005).
+// Nonzero magnitudes below 2^-120 (near the BF16 subnormal range, where the residual may be
+// inexact) take the exact fp64 product instead.  (A zero code gives an exact signed zero on
+// the fast path; a product that underflows fp32 to zero rounds to the same signed zero in
+// BF16.)
+// Source: q4k_mmq.rs, `dequant_nvfp4_to_bf16`.
+// =====================================================================================
+__device__ __forceinline__ float nv_e2m1(uint32_t c) {  // OCP FP4 E2M1
+    const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+    const float mag = e == 0 ? 0.5f * (float)m : __uint_as_float(((e + 126u) << 23) | (m << 22));
+    return (c & 8u) ? -mag : mag;
+}
+
+__device__ __forceinline__ float nv_e4m3(uint32_t b) {  // OCP FP8 E4M3 (0x7F / 0xFF: NaN)
+    const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+    float mag = e == 0 ? (float)m * 0.001953125f : __uint_as_float(((e + 120u) << 23) | (m << 20));
+    if (e == 15u && m == 7u) mag = __uint_as_float(0x7FC00000u);
+    return (b & 0x80u) ? -mag : mag;
+}
+
+// Fast path: BF16 bits of the product, and whether it needs the exact path instead.
+__device__ __forceinline__ uint32_t nv_bf16_fast(float a, float s2, uint32_t& tiny) {
+    const float p = __fmul_rz(a, s2);
+    const float r = __fmaf_rn(a, s2, -p);  // exact residual of the truncated product
+    tiny = (p != 0.0f && fabsf(p) < 0x1p-120f) ? 1u : 0u;
+    const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(__float_as_uint(p) | (r != 0.0f ? 1u : 0u)));
+    return *reinterpret_cast<const uint16_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t nv_bf16_exact(float a, float s2) {
+    const __nv_bfloat16 h = __double2bfloat16((double)a * (double)s2);  // exact product (<= 30 bits)
+    return *reinterpret_cast<const uint16_t*>(&h);
+}
+
+__global__ void __launch_bounds__(256) nvfp4_dequant_kernel(const uint8_t* __restrict__ packed,
+                                                            const uint8_t* __restrict__ scales,
+                                                            uint16_t* __restrict__ out, float scale2, int k) {
+    const int64_t r = blockIdx.x;
+    const uint8_t* prow = packed + r * (k / 2);
+    const uint8_t* srow = scales + r * (k / 16);
+    uint16_t* orow = out + r * k;
+    for (int g = threadIdx.x; g < k / 16; g += blockDim.x) {  // 16 values: 8 code bytes, 1 scale
+        const uint2 c = *reinterpret_cast<const uint2*>(prow + 8 * g);
+        const float sc = nv_e4m3(srow[g]);
+        float a[16];
+        uint32_t o[8], tiny = 0;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const uint32_t byte = ((j < 4 ? c.x : c.y) >> (8 * (j & 3))) & 0xFFu;
+            a[2 * j] = nv_e2m1(byte & 15u) * sc;  // exact
+            a[2 * j + 1] = nv_e2m1(byte >> 4) * sc;
+            uint32_t t0, t1;
+            o[j] = nv_bf16_fast(a[2 * j], scale2, t0) | (nv_bf16_fast(a[2 * j + 1], scale2, t1) << 16);
+            tiny |= (t0 << (2 * j)) | (t1 << (2 * j + 1));
+        }
+        if (__any_sync(__activemask(), tiny != 0u)) {  // rare: redo the tiny products exactly
+#pragma unroll
+            for (int e = 0; e < 16; e++) {
+                if ((tiny >> e) & 1u) {
+                    const uint32_t v = nv_bf16_exact(a[e], scale2);
+                    o[e >> 1] = (e & 1) ? ((o[e >> 1] & 0xFFFFu) | (v << 16)) : ((o[e >> 1] & 0xFFFF0000u) | v);
+                }
+            }
+        }
+        uint4* dst = reinterpret_cast<uint4*>(orow + 16 * g);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+// =====================================================================================
 // SiLU(gate) * up -> BF16 (silu_mul1 in common.cuh).
 // Source: dense_ffn_decode_batch.rs, `forward_km_q2` (`silu_mul`).
 // =====================================================================================
@@ -287,6 +364,20 @@ int quantize_act_q8_1(const uint16_t* x, void* act_q8, uint32_t m, uint32_t k, b
     else
         q8_1_kernel<false><<<grid_for(work, 256), 256, 0, (cudaStream_t)stream>>>(x, codes, ds, m, k, kp);
     return check_launch("quantize_act_q8_1");
+}
+
+int dequant_nvfp4_to_bf16(const void* packed, const void* scales, uint16_t* out, float scale2, uint32_t n,
+                          uint32_t k, bq_stream_t stream) {
+    const char* who = "dequant_nvfp4_to_bf16";
+    if (k % 16 != 0) return fail(BQ_ERR_INVALID, "%s: k = %u must be a multiple of 16", who, k);
+    if (n == 0 || k == 0) return ok();
+    if (!packed || !scales || !out) return fail(BQ_ERR_INVALID, "%s: NULL pointer", who);
+    if (!aligned16(packed) || !aligned16(out))
+        return fail(BQ_ERR_INVALID, "%s: packed and out must be 16-byte aligned", who);
+    if (n > 0x7FFFFFFFu || k > (1u << 30)) return fail(BQ_ERR_INVALID, "%s: shape too large", who);
+    nvfp4_dequant_kernel<<<n, 256, 0, (cudaStream_t)stream>>>((const uint8_t*)packed, (const uint8_t*)scales, out,
+                                                              scale2, (int)k);
+    return check_launch(who);
 }
 
 int silu_mul_bf16(const uint16_t* gate, const uint16_t* up, uint16_t* out, size_t count, bq_stream_t stream) {

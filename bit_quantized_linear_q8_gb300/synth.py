@@ -119,3 +119,20 @@ def small_dense(seed: int, n: int, k: int, m: int, std: float = WEIGHT_STD):
     w = dense_weight(g, n, k, std)
     x = activations(g, m, k)
     return dict(n=n, k=k, m=m, w=w, x=x)
+
+
+def nvfp4_weight(seed: int, n: int, k: int):
+    """A synthetic NVFP4 weight: uniform random E2M1 code bytes [n, k/2], E4M3 scale bytes
+    [n, k/16] drawn from the positive normal codes with exponent fields 4..11 (scales
+    2^-3 .. 2^4, as a per-16 amax / 6 of unit-scale weights), and a per-tensor scale2."""
+    g = _gen(seed)
+    packed = torch.randint(0, 256, (n, k // 2), generator=g, dtype=torch.int32).to(torch.uint8).numpy()
+    ex = torch.randint(4, 12, (n, k // 16), generator=g, dtype=torch.int32)
+    mant = torch.randint(0, 8, (n, k // 16), generator=g, dtype=torch.int32)
+    scales = ((ex << 3) | mant).to(torch.uint8).numpy()
+    return dict(n=n, k=k, packed=packed, scales=scales, scale2=0.0021)
+
+
+def nvfp4_ffn_weight():
+    """The Q4_K FFN weight source shape: gate/up projection [17408, 5120] in NVFP4."""
+    return nvfp4_weight(5, 17408, 5120)

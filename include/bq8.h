@@ -170,6 +170,18 @@ int q4k_mmq_gemm(const void* act_q8, const void* w_q4k, uint16_t* out, uint32_t 
  * caller's scratch, then a dense BF16 GEMM). */
 int dequant_q2_to_bf16(const bq_q2_weight* w, uint16_t* out, bq_stream_t stream);
 
+/* Dequantise an NVFP4 weight [n][k] to BF16 out[n][k] (the weight-preparation step before
+ * quantize_weight_q4k):  w = e2m1(code) * e4m3(scale) * scale2, the exact product rounded
+ * once to BF16 (round to nearest even).
+ *   packed: [n][k/2] bytes of OCP FP4 E2M1 codes, value 2j of a row in the low nibble of
+ *           byte j, value 2j + 1 in the high nibble (16-byte aligned);
+ *   scales: [n][k/16] OCP FP8 E4M3 bytes, one per 16 consecutive values of a row;
+ *   scale2: the per-tensor fp32 scale;  out: 16-byte aligned.  k % 16 == 0.
+ * A NaN scale byte (0x7F, 0xFF) gives a NaN output whose bit pattern is not specified.
+ * Source: q4k_mmq.rs, `dequant_nvfp4_to_bf16` (grid [n], block 256). */
+int dequant_nvfp4_to_bf16(const void* packed, const void* scales, uint16_t* out, float scale2, uint32_t n, uint32_t k,
+                          bq_stream_t stream);
+
 /* ---------------------------------------------------------------- diagnostics */
 
 /* Message for the calling thread's last failed call ("" after a successful call). */

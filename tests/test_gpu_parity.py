@@ -88,6 +88,38 @@ def test_q8_1_edge_values(B):
     assert np.array_equal(out, O.quantize_q8_1(bits))
 
 
+# ------------------------------------------------------------------------------ NVFP4 -> BF16
+def _nvfp4(B, d, scale2=None):
+    import torch
+    s2 = d["scale2"] if scale2 is None else scale2
+    out = B.dequant_nvfp4_to_bf16(torch.from_numpy(d["packed"]).cuda(), torch.from_numpy(d["scales"]).cuda(), s2,
+                                  d["n"], d["k"])
+    return bf16_dev_to_u16(out), O.dequant_nvfp4(d["packed"], d["scales"], s2, d["n"], d["k"])
+
+
+@pytest.mark.parametrize("n,k", [(1, 16), (3, 32), (37, 320), (300, 5120)])
+def test_nvfp4_dequant_bitexact(B, n, k):
+    out, ref = _nvfp4(B, synth.nvfp4_weight(800 + n, n, k))
+    assert np.array_equal(out, ref)
+
+
+def test_nvfp4_dequant_edges(B):
+    d = synth.nvfp4_weight(850, 6, 64)
+    sc = d["scales"]
+    sc[0] = [0x01, 0x02, 0x03, 0x07]            # E4M3 subnormal scales
+    sc[1] = [0x00, 0x80, 0x08, 0x7E]            # +-0, the smallest normal, the largest value (448)
+    sc[2] = [0xB8, 0xC0, 0xF0, 0xFE]            # negative scales
+    d["packed"][3] = 0x88                        # every code -0
+    for s2 in (d["scale2"], 3e-39, 1e-30, 1.0, 1e36):  # BF16 subnormal products (exact fp64 path) ... overflow to inf
+        out, ref = _nvfp4(B, d, s2)
+        assert np.array_equal(out, ref), s2
+
+
+def test_nvfp4_dequant_full(B):
+    out, ref = _nvfp4(B, synth.nvfp4_ffn_weight())
+    assert np.array_equal(out, ref)
+
+
 # ------------------------------------------------------------------------------ SiLU * mul
 def test_silu_mul_within_one_ulp(B):
     rng = np.random.default_rng(7)
