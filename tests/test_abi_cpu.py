@@ -95,6 +95,13 @@ def test_status_codes_without_launch(L):
     assert L.q4k_mmq_gemm(ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000), ctypes.c_void_p(0x4000), 4, 8, 300,
                           null) == 1
     assert b"multiple of 256" in L.bq_last_error()
+    # NVFP4 dequant: k % 16 == 0, 16-byte aligned codes and output; empty work is a no-op
+    a, b, c = ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000), ctypes.c_void_p(0x4000)
+    assert L.dequant_nvfp4_to_bf16(a, b, c, ctypes.c_float(1.0), 4, 40, null) == 1
+    assert b"multiple of 16" in L.bq_last_error()
+    assert L.dequant_nvfp4_to_bf16(ctypes.c_void_p(0x2008), b, c, ctypes.c_float(1.0), 4, 64, null) == 1
+    assert L.dequant_nvfp4_to_bf16(null, b, c, ctypes.c_float(1.0), 4, 64, null) == 1
+    assert L.dequant_nvfp4_to_bf16(null, null, null, ctypes.c_float(1.0), 0, 64, null) == _abi.BQ_OK
 
 
 def test_python_binding_refuses_cpu_tensors(L):
