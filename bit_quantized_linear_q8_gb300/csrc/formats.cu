@@ -1,7 +1,10 @@
-// formats.cu -- weight packing, dequantisation, activation quantisation and SiLU*mul.
+// formats.cu -- weight packing, dequantisation (Q2_0 and NVFP4 to BF16), activation
+// quantisation (q8_1), the Q4_K weight quantiser and SiLU*mul.
 //
-// All of these are HBM-bound streaming kernels: coalesced 8/16-byte accesses, grid sized
-// as a multiple of the SM count, no shared memory.
+// All of these are streaming kernels without shared memory: coalesced 8/16-byte accesses,
+// grids sized as a multiple of the SM count (the NVFP4 dequant keeps the page's one CTA per
+// row).  The q8_1 quantiser is bound by instruction issue (one IEEE division per value for
+// the bit-exact rounding), the others by memory.
 #include "common.cuh"
 
 namespace bq8 {
