@@ -65,6 +65,7 @@ def lib():
             "orc_e4m3_value": (ctypes.c_double, [ctypes.c_int]),
             "orc_dequant_nvfp4": (None, [P, P, ctypes.c_float, I, I, P]),
             "orc_num_threads": (ctypes.c_int, []),
+            "orc_set_num_threads": (None, [ctypes.c_int]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -80,6 +81,11 @@ def _p(a):
 
 def _c(a, dtype):
     return np.ascontiguousarray(a, dtype=dtype)
+
+
+def set_num_threads(n: int) -> None:
+    """Threads used by the oracle's parallel loops from now on."""
+    lib().orc_set_num_threads(int(n))
 
 
 def num_threads() -> int:

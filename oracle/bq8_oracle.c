@@ -474,6 +474,15 @@ void orc_dequant_nvfp4(const uint8_t* packed, const uint8_t* scales, float scale
         }
 }
 
+/* Threads the oracle's parallel loops use from now on (timing on one core). */
+void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 int orc_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();
