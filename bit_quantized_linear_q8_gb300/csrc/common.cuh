@@ -45,7 +45,13 @@ int make_tmap_3d_u8(CUtensorMap* map, const void* base, const uint64_t (&dims)[3
 // Reads and clears each translation unit's device status word (nonzero after a bounded
 // wait gave up).
 unsigned int gemv_status_take();
+unsigned int gemv_hm_status_take();
 unsigned int mmq_tc_status_take();
+
+// The FP16 warp-MMA GEMV (gemv_hm.cu) and the shapes it takes.
+bool gemv_hm_supported(const bq_q2_weight* w, uint32_t m);
+int launch_q2_gemv_hm(const uint16_t* x, const bq_q2_weight* w, uint16_t* y, uint32_t m, uint16_t* hgate,
+                      cudaStream_t stream, const char* who);
 
 // ------------------------------------------------------------------ device helpers
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
@@ -140,6 +146,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     for (uint32_t it = 0; it < (1u << 26); it++) {
         __nanosleep(32);
         if (mbar_test(bar, parity)) return true;
+    }
+    return false;
+}
+
+// Waits for phase `parity` of `bar` with mbarrier.try_wait, which suspends the warp in
+// hardware until the phase completes (or a system time limit of microseconds passes), so a
+// waiting warp takes no issue slots.  Gives up (false) after 2^20 tries (well over a second).
+__device__ __forceinline__ bool mbar_wait_suspend(uint64_t* bar, uint32_t parity) {
+    for (uint32_t it = 0; it < (1u << 20); it++) {
+        uint32_t done;
+        asm volatile(
+            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        if (done) return true;
     }
     return false;
 }

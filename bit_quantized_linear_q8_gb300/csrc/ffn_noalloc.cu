@@ -24,12 +24,43 @@ static __device__ __align__(256) uint16_t g_ffn_scratch[2 * BQ_FFN_NOALLOC_MAX_E
 
 constexpr int FFN_NOALLOC_MAX_DEVICES = 64;
 
+typedef CUresult (*PFN_ctxGetCurrent)(CUcontext*);
+typedef CUresult (*PFN_ctxGetId)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (0 if the driver cannot say).  A
+// context created after cudaDeviceReset gets a new id, so an address cached for the old one
+// is looked up again.
+static unsigned long long current_context_id() {
+    static PFN_ctxGetCurrent get_current = nullptr;
+    static PFN_ctxGetId get_id = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_ctxGetCurrent>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_ctxGetId>(p);
+        tried = true;
+    }
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, &id) == CUDA_SUCCESS)
+        return id;
+    return 0;
+}
+
 // Device address of g_ffn_scratch on the current device.  In host code the array's name
-// is only a host-side shadow, so the address is looked up once per device with that
-// device current and cached; later calls do no CUDA runtime work here.
+// is only a host-side shadow, so the address is looked up with that device current the
+// first time a device is used (and again if its context was replaced) and cached; later
+// calls do no CUDA runtime work here beyond reading the context id.
 static int scratch_address(uint16_t** out, const char* who) {
     static std::mutex mu;
     static uint16_t* addr[FFN_NOALLOC_MAX_DEVICES] = {};
+    static unsigned long long ctx_id[FFN_NOALLOC_MAX_DEVICES] = {};
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0)
         return fail(BQ_ERR_DEVICE, "%s: no current CUDA device", who);
@@ -37,7 +68,8 @@ static int scratch_address(uint16_t** out, const char* who) {
         return fail(BQ_ERR_UNSUPPORTED, "%s: device ordinal %d is beyond the %d this entry point tracks", who, dev,
                     FFN_NOALLOC_MAX_DEVICES);
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    const unsigned long long id = addr[dev] ? current_context_id() : 0;
+    if (!addr[dev] || (id != 0 && id != ctx_id[dev])) {
         void* p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_ffn_scratch);
         if (e != cudaSuccess || !p) {
@@ -47,6 +79,7 @@ static int scratch_address(uint16_t** out, const char* who) {
             return fail(code, "%s: cudaGetSymbolAddress of the scratch array failed: %s", who, cudaGetErrorString(e));
         }
         addr[dev] = static_cast<uint16_t*>(p);
+        ctx_id[dev] = current_context_id();  // the context cudaGetSymbolAddress made current
     }
     *out = addr[dev];
     return BQ_OK;

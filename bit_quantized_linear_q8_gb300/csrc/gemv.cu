@@ -579,6 +579,7 @@ int launch_q2_gemv(const uint16_t* x, const bq_q2_weight* w, uint16_t* y, uint32
             return fail(BQ_ERR_LAUNCH, "%s: memset failed", who);
         return ok();
     }
+    if (gemv_hm_supported(w, m)) return launch_q2_gemv_hm(x, w, y, m, hgate, stream, who);
     return launch_q2_gemv_mma(x, w, y, m, hgate, allow_split, stream, who);
 }
 

@@ -139,7 +139,8 @@ int ffn_q2_km(const uint16_t* x, const bq_q2_weight* gate, const bq_q2_weight* u
  *    launched); every other check is ffn_q2_km's.
  *  - The first call on each device looks up the array's device address with that device
  *    current (cudaGetSymbolAddress) and caches it; make that first call before any stream
- *    capture on the device.
+ *    capture on the device.  If the device's context is replaced (cudaDeviceReset), the
+ *    next call looks the address up again, so make that call before any capture too.
  *  - The array is shared by every call in the process and keeps the last call's contents;
  *    calls that overlap on the GPU (other streams or host threads) race on it.  Calls on
  *    one stream are ordered and safe.  The array stays allocated on every GPU that loaded

@@ -7,6 +7,10 @@ import numpy as np
 REL_TOL = 2e-3
 ABS_TOL = 1e-3
 
+# (what, fraction of outputs that are a BF16 neighbour of the fp64 reference) for every
+# tolerance check of the session; tests/conftest.py prints them after the run.
+FAITHFUL_REPORT = []
+
 
 def bf16_half_ulp(a):
     a = np.abs(np.asarray(a, np.float64))
@@ -26,7 +30,20 @@ def check_bf16_vs_f64(y_bits, ref, what=""):
         idx = np.argwhere(bad)[:5]
         raise AssertionError("%s: %d of %d outside tolerance; e.g. %s" % (
             what, int(bad.sum()), bad.size, [(tuple(i), float(y[tuple(i)]), float(ref[tuple(i)])) for i in idx]))
-    return faithful_fraction(y, ref)
+    frac = faithful_fraction(y, ref)
+    FAITHFUL_REPORT.append((what, frac, int(y.size), float((err / np.maximum(bound, 1e-300)).max()) if y.size else 0.0))
+    return frac
+
+
+def tile_quadrant_rows(m, seed, extra=()):
+    """Rows that hit every 128-row tile and, inside it, every 32-row quadrant (the tensor
+    memory lane quadrant of an M = 128 MMA) at least once, plus the first and last row and
+    `extra`; seeded, sorted and unique."""
+    rng = np.random.default_rng(seed)
+    rows = [0, m - 1] + list(extra)
+    for base in range(0, m, 32):
+        rows.append(base + int(rng.integers(0, min(32, m - base))))
+    return np.unique(np.asarray(rows, np.int64))
 
 
 def faithful_fraction(y, ref):

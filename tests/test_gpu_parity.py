@@ -10,7 +10,7 @@ import pytest
 
 import oracle as O
 from bit_quantized_linear_q8_gb300 import synth
-from helpers import (bf16_dev_to_u16, check_bf16_vs_f64, to_dev_u16_as_bf16, to_dev_u8, u8_dev)
+from helpers import (bf16_dev_to_u16, check_bf16_vs_f64, tile_quadrant_rows, to_dev_u16_as_bf16, to_dev_u8, u8_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -179,6 +179,51 @@ def test_gemv_closed_forms(B):
     assert np.array_equal(y, deq[:, 201])
 
 
+@pytest.mark.parametrize("m", [1, 4])
+def test_gemv_exact_differential(B, m):
+    # integer activations (|x| <= 127, exact in BF16) and power-of-two group scales: every
+    # product and partial sum is an exact binary value, so the stored BF16 must be the
+    # round-to-nearest-even of the exact product, bit for bit
+    import torch
+    rng = np.random.default_rng(20 + m)
+    n, k = 300, 1024
+    xi = rng.integers(-127, 128, size=(m, k))
+    codes = rng.integers(0, 4, size=(n, k)).astype(np.uint8)
+    sexp = rng.integers(-6, -1, size=(n, k // 128))
+    scales = torch.tensor(np.exp2(sexp).astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    xb = torch.tensor(xi.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    w = dev_q2(B, codes, scales)
+    y = bf16_dev_to_u16(B.q2_gemv_batchm(to_dev_u16_as_bf16(xb), w))
+    exact = O.q2_gemv(xb, O.q2_pack(codes, scales), n, k)
+    assert np.array_equal(y, O.f64_to_bf16(exact))
+
+
+def test_gemv_m1_activation_range(B):
+    """The one-row GEMV holds activations as 16-bit fixed point per row: rows with a wide
+    dynamic range, a single tiny nonzero value, all zeros, and a negative maximum."""
+    import torch
+    n, k = 200, 1024
+    d = synth.small_q2(470, n, k, 1)
+    w = dev_q2(B, d["codes"], d["scales"])
+    packed = O.q2_pack(d["codes"], d["scales"])
+    rng = np.random.default_rng(3)
+    cases = {
+        "wide range": rng.standard_normal(k) * np.exp2(rng.integers(-30, 12, size=k)),
+        "one tiny value": np.where(np.arange(k) == 77, 3e-30, 0.0),
+        "zeros": np.zeros(k),
+        "negative max": np.where(np.arange(k) == 5, -6.0e4, rng.standard_normal(k)),
+        "large": rng.standard_normal(k) * 1e30,
+    }
+    for what, xv in cases.items():
+        xb = torch.tensor(xv[None, :].astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        y = bf16_dev_to_u16(B.q2_gemv(to_dev_u16_as_bf16(xb), w))
+        ref = O.q2_gemv(xb, packed, n, k)
+        if what == "zeros":
+            assert not np.any(y & 0x7FFF), what
+        else:
+            check_bf16_vs_f64(y, ref, "gemv m=1 " + what)
+
+
 def test_gemv_q2_gemv_1024(B):
     d = synth.q2_gemv_1024()
     w = dev_q2(B, d["codes"], d["scales"])
@@ -252,17 +297,18 @@ def _ffn_check(B, x, gate, up, down, hidden, inter):
     assert np.all(np.abs(y - y_ref) <= bound_y), "ffn out: %d outside" % int((np.abs(y - y_ref) > bound_y).sum())
 
 
-def test_ffn_small(B):
+@pytest.mark.parametrize("m", [1, 3])
+def test_ffn_small(B, m):
     hidden, inter = 256, 640
     g0 = synth._gen(500)
     gate = synth.q2_codes_scales(g0, inter, hidden)
     up = synth.q2_codes_scales(g0, inter, hidden)
     down = synth.q2_codes_scales(g0, hidden, inter)
-    x = synth.activations(g0, 3, hidden)
+    x = synth.activations(g0, m, hidden)
     _ffn_check(B, x, gate, up, down, hidden, inter)
 
 
-@pytest.mark.parametrize("m", [2, 3, 8])
+@pytest.mark.parametrize("m", [1, 2, 3, 8])
 def test_ffn_decode_full(B, m):
     d = synth.ffn_q2_decode()
     _ffn_check(B, d["x"][:m], d["gate"], d["up"], d["down"], d["hidden"], d["inter"])
@@ -318,7 +364,6 @@ def test_q2_mmq_exact_differential(B):
 
 @pytest.mark.parametrize("m", [512, 2048, 4096])
 def test_q2_mmq_prefill_full(B, m):
-    import torch
     d = synth.q2_prefill_weight()
     x = synth.q2_prefill_x(m)
     w = dev_q2(B, d["codes"], d["scales"])
@@ -327,21 +372,28 @@ def test_q2_mmq_prefill_full(B, m):
     act_ref = O.quantize_q8_1(x)
     assert np.array_equal(u8_dev(act), act_ref)
     packed = O.q2_pack(d["codes"], d["scales"])
-    if m == 512:
-        rows = np.arange(m)
-    else:  # sampled rows: the outlier rows plus a seeded sample, each computed in full
-        amax = np.abs(O.bf16_to_f32(x)).max(axis=1)
-        out_rows = np.argsort(-amax)[: max(1, m // 100)]
-        rows = np.unique(np.concatenate([out_rows, np.random.default_rng(m).choice(m, 48, replace=False), [0, m - 1]]))
+    # every 128-row tile and every 32-row lane quadrant of it, plus the outlier rows
+    amax = np.abs(O.bf16_to_f32(x)).max(axis=1)
+    rows = tile_quadrant_rows(m, m, extra=np.argsort(-amax)[: max(1, m // 100)])
     ref = O.q2_mmq(act_ref, packed, m, d["n"], d["k"], rows=rows)
     check_bf16_vs_f64(y[rows], ref, "q2 mmq prefill m=%d" % m)
-    # the dequant + dense GEMM route computes the same projection (different rounding of
-    # the activations: BF16 instead of q8_1), so compare it loosely on the same rows
-    wd = B.dequant_q2_to_bf16(w)
-    yd = (to_dev_u16_as_bf16(x[rows]).float() @ wd.float().t()).double().cpu().numpy()
-    yv = (y[rows].astype(np.uint32) << 16).view(np.float32)
-    rel = np.linalg.norm(yv - yd) / np.linalg.norm(yd)
-    assert rel < 1e-2
+
+
+@pytest.mark.parametrize("m", [512, 2048])
+def test_dequant_gemm_prefill_full(B, m):
+    """The fallback route (dequantise to BF16, then the dense BF16 GEMM) against the fp64
+    product of the BF16 activations and the dequantised weight, element by element on rows
+    that hit every 128-row tile and lane quadrant."""
+    d = synth.q2_prefill_weight()
+    x = synth.q2_prefill_x(m)
+    w = dev_q2(B, d["codes"], d["scales"])
+    out, mode = B.q2_prefill_proj(to_dev_u16_as_bf16(x), w, mode="dequant")
+    assert mode == "dequant"
+    y = bf16_dev_to_u16(out)
+    amax = np.abs(O.bf16_to_f32(x)).max(axis=1)
+    rows = tile_quadrant_rows(m, 7 * m, extra=np.argsort(-amax)[: max(1, m // 100)])
+    ref = O.q2_gemv(x[rows], O.q2_pack(d["codes"], d["scales"]), d["n"], d["k"])
+    check_bf16_vs_f64(y[rows], ref, "dequant + gemm m=%d" % m)
 
 
 # ------------------------------------------------------------------------------ Q4_K MMQ
@@ -356,12 +408,11 @@ def test_q4k_mmq_small(B, m, n, k):
 
 
 def test_q4k_ffn_prefill_full(B):
-    """The FFN prefill at m = 2048 (gate and up MMQ, SiLU*mul, q8_1 of h, down MMQ).
-    Gate and up are checked on sampled rows against the oracle on the same q8_1 input; the
-    down GEMM is checked at its full k = 17408 on the oracle's own h for those rows (uploaded
-    and quantised on the GPU, bit-exact); the kernel chain's own output is compared loosely
-    with the oracle chain (a sanity check: the two h differ by BF16 rounding)."""
-    import torch
+    """The FFN prefill at m = 2048 (gate and up MMQ, SiLU*mul, q8_1 of h, down MMQ), stage
+    by stage and element by element on rows that hit every 128-row tile and lane quadrant:
+    gate and up against the oracle on the same q8_1 input; h against the oracle's SiLU*mul
+    of the kernels' own g and u (within one BF16 step); the q8_1 of h bit for bit; and the
+    chain's output against the oracle's down GEMM of the kernels' own h."""
     d = synth.q4k_ffn_prefill()
     m, hidden, inter = d["m"], d["hidden"], d["inter"]
     wq = {kk: B.quantize_weight_q4k(to_dev_u16_as_bf16(d[kk])) for kk in ("w_gate", "w_up", "w_down")}
@@ -374,19 +425,22 @@ def test_q4k_ffn_prefill_full(B):
     gt = B.q4k_mmq_gemm(a1, wq["w_gate"], m, inter, hidden)
     ut = B.q4k_mmq_gemm(a1, wq["w_up"], m, inter, hidden)
     h = B.silu_mul_bf16(gt, ut)
-    out = B.q4k_mmq_gemm(B.quantize_act_q8_1(h), wq["w_down"], m, hidden, inter)
-    rows = np.unique(np.concatenate([np.random.default_rng(5).choice(m, 14, replace=False), [0, m - 1]]))
+    a2 = B.quantize_act_q8_1(h)
+    out = B.q4k_mmq_gemm(a2, wq["w_down"], m, hidden, inter)
+    rows = tile_quadrant_rows(m, 5)
     g_ref = O.q4k_mmq(a1_ref, wq_ref["w_gate"], m, inter, hidden, rows=rows)
     u_ref = O.q4k_mmq(a1_ref, wq_ref["w_up"], m, inter, hidden, rows=rows)
-    check_bf16_vs_f64(bf16_dev_to_u16(gt)[rows], g_ref, "q4k gate")
-    check_bf16_vs_f64(bf16_dev_to_u16(ut)[rows], u_ref, "q4k up")
-    # oracle chain for the sampled rows: BF16 g, u -> BF16 h -> q8_1 -> down
-    h_ref = O.silu_mul_bf16(O.f64_to_bf16(g_ref), O.f64_to_bf16(u_ref))
-    a2_ref = O.quantize_q8_1(h_ref)
+    g_bits, u_bits = bf16_dev_to_u16(gt)[rows], bf16_dev_to_u16(ut)[rows]
+    check_bf16_vs_f64(g_bits, g_ref, "q4k gate")
+    check_bf16_vs_f64(u_bits, u_ref, "q4k up")
+    h_bits = bf16_dev_to_u16(h)[rows]
+    h_or = O.silu_mul_bf16(g_bits, u_bits)
+    step = np.abs(h_bits.astype(np.int32) - h_or.astype(np.int32))
+    assert step.max() <= 1 and np.mean(step == 0) > 0.99
+    # q8_1 of the kernels' h, the rows picked out of the planar buffer
+    a2_ref = O.quantize_q8_1(h_bits)
+    c_dev, ds_dev = O.q8_1_views(u8_dev(a2), m, inter)
+    c_ref, ds_ref = O.q8_1_views(a2_ref, len(rows), inter)
+    assert np.array_equal(c_dev[rows], c_ref) and np.array_equal(ds_dev[rows], ds_ref)
     y_ref = O.q4k_mmq(a2_ref, wq_ref["w_down"], len(rows), hidden, inter)
-    a2 = B.quantize_act_q8_1(to_dev_u16_as_bf16(h_ref))
-    assert np.array_equal(u8_dev(a2), a2_ref)
-    y_down = bf16_dev_to_u16(B.q4k_mmq_gemm(a2, wq["w_down"], len(rows), hidden, inter))
-    check_bf16_vs_f64(y_down, y_ref, "q4k down (k=17408)")
-    yv = (bf16_dev_to_u16(out)[rows].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    assert np.linalg.norm(yv - y_ref) / np.linalg.norm(y_ref) < 1e-2
+    check_bf16_vs_f64(bf16_dev_to_u16(out)[rows], y_ref, "q4k chain out (down, k=17408)")
