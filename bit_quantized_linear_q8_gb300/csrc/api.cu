@@ -1,6 +1,9 @@
 // api.cu -- status handling, size helpers and shared host checks of the libbq8 C ABI.
 #include <stdarg.h>
 #include <stdio.h>
+#include <string.h>
+
+#include <mutex>
 
 #include "common.cuh"
 
@@ -89,6 +92,57 @@ int make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t ro
                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(BQ_ERR_INVALID, "%s: tensor map encoding failed (CUresult %d)", who, (int)r);
+    return BQ_OK;
+}
+
+// Encoded 2-D byte tensor maps, keyed by everything the encoding depends on (base address,
+// shape, stride, box, swizzle, device), so repeated calls on the same weight encode nothing.
+// The map describes only addresses and shapes, never contents, so a cached entry stays valid
+// for any data later placed at that address.  128 entries, replaced round-robin.
+int cached_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint64_t stride_bytes,
+                      uint32_t box_bytes, uint32_t box_rows, bool swizzle128, const char* who) {
+    struct Entry {
+        const void* base;
+        uint64_t row_bytes, rows, stride;
+        uint32_t box_bytes, box_rows;
+        int swz, dev;
+        bool used;
+        CUtensorMap map;
+    };
+    constexpr int N = 128;
+    static Entry table[N];
+    static int next = 0;
+    static std::mutex mu;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < N; i++) {
+            const Entry& e = table[i];
+            if (e.used && e.base == base && e.row_bytes == row_bytes && e.rows == rows && e.stride == stride_bytes &&
+                e.box_bytes == box_bytes && e.box_rows == box_rows && e.swz == (int)swizzle128 && e.dev == dev) {
+                *map = e.map;
+                return BQ_OK;
+            }
+        }
+    }
+    CUtensorMap fresh;
+    const int st = make_tmap_2d_u8(&fresh, base, row_bytes, rows, stride_bytes, box_bytes, box_rows, swizzle128, who);
+    if (st) return st;
+    std::lock_guard<std::mutex> lock(mu);
+    Entry& e = table[next];
+    next = (next + 1) % N;
+    e.base = base;
+    e.row_bytes = row_bytes;
+    e.rows = rows;
+    e.stride = stride_bytes;
+    e.box_bytes = box_bytes;
+    e.box_rows = box_rows;
+    e.swz = (int)swizzle128;
+    e.dev = dev;
+    e.map = fresh;
+    e.used = true;
+    *map = fresh;
     return BQ_OK;
 }
 

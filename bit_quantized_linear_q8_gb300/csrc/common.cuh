@@ -37,6 +37,10 @@ int make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t row_bytes, uint
 int make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t row_elems, uint64_t rows,
                  uint64_t stride_bytes, uint32_t box_elems, uint32_t box_rows, bool swizzle128, const char* who);
 
+// make_tmap_2d_u8 through a small process-wide cache (no encoding on a hit).
+int cached_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint64_t stride_bytes,
+                      uint32_t box_bytes, uint32_t box_rows, bool swizzle128, const char* who);
+
 // 3-D tiled TMA descriptor over bytes: dims {d0, d1, d2}, byte strides of d1 and d2 (any
 // order, multiples of 16), box {b0, b1, b2} (b0 a multiple of 16), no swizzle.
 int make_tmap_3d_u8(CUtensorMap* map, const void* base, const uint64_t (&dims)[3], const uint64_t (&strides)[2],
@@ -152,9 +156,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 
 // Waits for phase `parity` of `bar` with mbarrier.try_wait, which suspends the warp in
 // hardware until the phase completes (or a system time limit of microseconds passes), so a
-// waiting warp takes no issue slots.  Gives up (false) after 2^20 tries (well over a second).
+// waiting warp takes no issue slots.  Gives up (false) once 20 ms have passed on the global
+// timer (a copy of a few kilobytes takes microseconds), or after 2^22 tries.
 __device__ __forceinline__ bool mbar_wait_suspend(uint64_t* bar, uint32_t parity) {
-    for (uint32_t it = 0; it < (1u << 20); it++) {
+    uint64_t start = 0;
+    for (uint32_t it = 0; it < (1u << 22); it++) {
         uint32_t done;
         asm volatile(
             "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
@@ -162,6 +168,12 @@ __device__ __forceinline__ bool mbar_wait_suspend(uint64_t* bar, uint32_t parity
             : "r"(smem_u32(bar)), "r"(parity)
             : "memory");
         if (done) return true;
+        if ((it & 63) == 63) {
+            uint64_t now;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+            if (start == 0) start = now;
+            else if (now - start > 20000000ull) return false;
+        }
     }
     return false;
 }
