@@ -315,7 +315,7 @@ def run_ours(args, rank, local, world):
 
     if rank != 0:
         return None
-    traffic = _traffic_record("bit_quantized_linear_q8_gb300/csrc/gemv.cu", "q2_gemv_qkvz")
+    traffic = _traffic_record("bit_quantized_linear_q8_gb300/csrc/gemv_hm.cu", "q2_gemv_qkvz")
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(elapsed_max / args.steps * 1e3, 4), "higher_is_better": True,
@@ -325,7 +325,7 @@ def run_ours(args, rank, local, world):
                    "parallelism": "replicas x%d" % world, "graph": "one CUDA graph per step"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
-                     "kernel": "q2_gemv_kernel", "peak_source": peak_src,
+                     "kernel": "q2_gemv_hm_kernel", "peak_source": peak_src,
                      "note": "algorithmic bytes per launch (weight + x + y) / (graph elapsed / launches)"},
         "per_m": kern,
         "e2e": e2e,
@@ -415,7 +415,8 @@ def _rows_ffn(rows, reps, dev, hbm_peak):
                             for s in sets])
         t = _time_graph(g, reps) / len(sets)
         rows["a4_ffn_q2_m%d" % m] = {"us": t * 1e6, "weight_GBps": chain_bytes / t / 1e9,
-                                     "frac_hbm": chain_bytes / t / 1e9 / hbm_peak, "launches": 3}
+                                     "frac_hbm": chain_bytes / t / 1e9 / hbm_peak,
+                                     "launches": 2, "note": "gate+up in one launch (SiLU*mul in its store), then down"}
     # per-GEMV times inside the chain at m = 8 (gate, down) and SiLU*mul alone
     xm = xf.contiguous()
     gs = torch.empty((8, inter), dtype=torch.bfloat16, device=dev)

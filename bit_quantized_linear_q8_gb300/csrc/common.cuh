@@ -56,6 +56,11 @@ unsigned int mmq_tc_status_take();
 bool gemv_hm_supported(const bq_q2_weight* w, uint32_t m);
 int launch_q2_gemv_hm(const uint16_t* x, const bq_q2_weight* w, uint16_t* y, uint32_t m, uint16_t* hgate,
                       cudaStream_t stream, const char* who);
+// The dual form for an FFN's gate and up weights of the same shape: h = BF16(SiLU(g) * u)
+// into h and u into u, in one launch (gemv_hm.cu).
+bool gemv_hm_dual_supported(const bq_q2_weight* gate, uint32_t m);
+int launch_q2_gemv_hm_dual(const uint16_t* x, const bq_q2_weight* gate, const bq_q2_weight* up, uint16_t* h,
+                           uint16_t* u, uint32_t m, cudaStream_t stream, const char* who);
 
 // ------------------------------------------------------------------ device helpers
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }

@@ -631,9 +631,15 @@ int ffn_q2_km(const uint16_t* x, const bq_q2_weight* gate, const bq_q2_weight* u
     if (gs < us + inter_bytes && us < gs + inter_bytes)
         return fail(BQ_ERR_INVALID, "%s: gate_scratch and up_scratch overlap", who);
     cudaStream_t s = (cudaStream_t)stream;
-    if ((st = launch_q2_gemv(x, gate, gate_scratch, m, s, who))) return st;
-    // the up projection's epilogue also forms h = SiLU(g) * u in gate_scratch
-    if ((st = launch_q2_gemv(x, up, up_scratch, m, s, who, gate_scratch))) return st;
+    if (gate->n > 0 && gate->k > 0 && gate->group == up->group && gemv_hm_dual_supported(gate, m)) {
+        // one launch streams the gate and up weights together: u into up_scratch and
+        // h = SiLU(g) * u into gate_scratch, the same arithmetic as the two launches below
+        if ((st = launch_q2_gemv_hm_dual(x, gate, up, gate_scratch, up_scratch, m, s, who))) return st;
+    } else {
+        if ((st = launch_q2_gemv(x, gate, gate_scratch, m, s, who))) return st;
+        // the up projection's epilogue also forms h = SiLU(g) * u in gate_scratch
+        if ((st = launch_q2_gemv(x, up, up_scratch, m, s, who, gate_scratch))) return st;
+    }
     // The down projection runs without the cluster K split here: right after the up
     // projection a cluster launch loses its early start (measured: chain 54.9 us with the
     // split against 48.0 us without at m = 2, equal at m = 3), while on its own the split

@@ -64,8 +64,11 @@ unsigned int gemv_hm_status_take() {
 struct HmParams {
     const uint8_t* codes;    // [n][k/4]
     const uint16_t* scales;  // [n][k/group] BF16
+    const uint8_t* codes2;   // dual form: the up weight (same shape)
+    const uint16_t* scales2;
     const uint16_t* x;       // [m][k] BF16
-    uint16_t* y;             // [m][n] BF16
+    uint16_t* y;             // [m][n] BF16 (dual form: h = BF16(SiLU(g) * u))
+    uint16_t* y2;            // dual form: [m][n] BF16 u
     uint16_t* hgate;         // optional [m][n] BF16: replaced by BF16(SiLU(hgate) * y)
     int n, k, group;
     int tmax;                // tiles of the largest CTA
@@ -73,16 +76,25 @@ struct HmParams {
     int nstages;
 };
 
-// Shared-memory carve-up, identical on host and device (offsets from a 1024-aligned base).
+// Warps sharing a tile pair (each takes 1/parts of a chunk's pack blocks), from the tile
+// pairs per row group: tgb / 2 rounded up, or tgb in the dual (nw = 2) form.
+__host__ __device__ inline int hm_parts(int tgb, int nw) {
+    const int np = nw == 2 ? tgb : (tgb + 1) >> 1;
+    return np <= 2 ? HM_MAX_PARTS : np <= 4 ? 4 : 2;
+}
+
+// Shared-memory carve-up, identical on host and device (offsets from a 1024-aligned base);
+// nw = 2 for the dual (gate and up) form.
 struct HmLayout {
-    size_t ring, btab, scal, slot, misc, total;
-    __host__ __device__ HmLayout(int m, int k, int group, int tgb, int nstages, int tmax) {
+    size_t ring, btab, scal, scal_w, slot, misc, total;
+    __host__ __device__ HmLayout(int m, int k, int group, int tgb, int nstages, int tmax, int nw) {
         const size_t P = (size_t)k / 128, G = (size_t)k / group;
-        ring = 0;                                                       // [stage][2 halves][16 tgb rows][128 B]
-        btab = ring + (size_t)nstages * 2 * tgb * HM_BOX;               // [P][4 quads][m][4 lanes][16 B]
-        scal = btab + P * (size_t)m * 256;                              // CTA's scale rows (+ alignment)
-        slot = scal + (((size_t)tmax * 16 * G * 2 + 32 + 15) & ~size_t(15));  // [8 parts][16 tmax rows][m] fp32
-        misc = slot + (size_t)HM_MAX_PARTS * 16 * tmax * m * 4;         // barriers, row maxima, row scales
+        ring = 0;                                                       // [stage][nw][2 halves][16 tgb rows][128 B]
+        btab = ring + (size_t)nstages * nw * 2 * tgb * HM_BOX;          // [P][4 quads][m][4 lanes][16 B]
+        scal = btab + P * (size_t)m * 256;                              // [nw] CTA's scale rows (+ alignment)
+        scal_w = ((size_t)tmax * 16 * G * 2 + 32 + 15) & ~size_t(15);
+        slot = scal + nw * scal_w;                                      // [parts][nw][16 tmax rows][m] fp32
+        misc = slot + (size_t)hm_parts(tgb, nw) * nw * 16 * tmax * m * 4;  // barriers, row maxima, row scales
         total = misc + 2 * HM_MAX_STAGES * 8 + 8 + 8 * 4 * 2 + 1024;    // + alignment
     }
 };
@@ -176,13 +188,17 @@ __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"r"(HM_CWARPS * 32) : "memory");
 }
 
-template <int M>
+// DUAL: one launch over the gate and up weights of an FFN (same shape), the warp's tile pair
+// being gate tile t and up tile t; the store forms u and h = SiLU(g) * u.
+template <int M, bool DUAL>
 __global__ void __launch_bounds__(HM_THREADS, 1)
-    q2_gemv_hm_kernel(const __grid_constant__ CUtensorMap tmap, const HmParams p) {
+    q2_gemv_hm_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap2,
+                      const HmParams p) {
+    constexpr int NW = DUAL ? 2 : 1;  // weights streamed
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);  // the swizzled boxes need 1024-byte alignment
     const int n = p.n, k = p.k;
-    const HmLayout L(M, k, p.group, p.tgb, p.nstages, p.tmax);
+    const HmLayout L(M, k, p.group, p.tgb, p.nstages, p.tmax, NW);
     uint8_t* ring = smem + L.ring;
     uint8_t* btab = smem + L.btab;
     uint8_t* scal = smem + L.scal;
@@ -206,7 +222,7 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
     const int nkc = (P + 7) >> 3;               // 1024-column chunks per row group
     const int nch = ngrp * nkc;
     const uint32_t box_bytes = (uint32_t)TGB * HM_BOX;
-    const uint32_t stage_bytes = 2 * box_bytes;
+    const uint32_t stage_bytes = NW * 2 * box_bytes;  // [weight][half][box]
 
     // the CTA's scales: bytes [s_lo, s_hi) of the plane by one bulk copy, the rest (at most
     // 14 bytes at the end of the plane) by plain loads
@@ -228,15 +244,24 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
     }
     if (tid < 8) rowmax[tid] = 0u;
     if (tid == 32)
-        for (int64_t o = s_hi; o < s_end; o += 2)
-            *reinterpret_cast<uint16_t*>(scal + (o - s_lo)) = __ldg(reinterpret_cast<const uint16_t*>(splane + o));
+        for (int w = 0; w < NW; w++) {
+            const uint8_t* sp = w ? reinterpret_cast<const uint8_t*>(p.scales2) : splane;
+            for (int64_t o = s_hi; o < s_end; o += 2)
+                *reinterpret_cast<uint16_t*>(scal + w * L.scal_w + (o - s_lo)) =
+                    __ldg(reinterpret_cast<const uint16_t*>(sp + o));
+        }
     __syncthreads();  // the last barrier all 288 threads take
 
     if (warp == HM_CWARPS) {
         // ---- producer: weights need nothing from the previous kernel, so it starts at once
         if (lane == 0) {
-            mbar_arrive_expect_tx(sbar, (uint32_t)(s_hi - s_lo));
-            if (s_hi > s_lo) bulk_load(scal, splane + s_lo, (uint32_t)(s_hi - s_lo), sbar);
+            mbar_arrive_expect_tx(sbar, (uint32_t)(NW * (s_hi - s_lo)));
+            if (s_hi > s_lo) {
+                bulk_load(scal, splane + s_lo, (uint32_t)(s_hi - s_lo), sbar);
+                if (DUAL)
+                    bulk_load(scal + L.scal_w, reinterpret_cast<const uint8_t*>(p.scales2) + s_lo,
+                              (uint32_t)(s_hi - s_lo), sbar);
+            }
             bool ok = true;
             int nis = 0;  // chunks requested
             HmCursor cur = {0, 0, 0, 0u};
@@ -249,18 +274,21 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
                 // one box of 128 bytes x 16 TGB rows per 512-column half that starts inside the row
                 uint8_t* dst = ring + (size_t)cur.s * stage_bytes;
                 const int nh = cur.kc * 256 + 128 < kb ? 2 : 1;
-                mbar_arrive_expect_tx(&full[cur.s], (uint32_t)nh * box_bytes);
-                for (int h = 0; h < nh; h++)
-                    tma_load_2d(dst + (size_t)h * box_bytes, &tmap, cur.kc * 256 + h * 128, r0 + 16 * cur.gi * TGB,
-                                &full[cur.s]);
+                mbar_arrive_expect_tx(&full[cur.s], (uint32_t)(NW * nh) * box_bytes);
+                for (int w = 0; w < NW; w++)
+                    for (int h = 0; h < nh; h++)
+                        tma_load_2d(dst + (size_t)(w * 2 + h) * box_bytes, w ? &tmap2 : &tmap, cur.kc * 256 + h * 128,
+                                    r0 + 16 * cur.gi * TGB, &full[cur.s]);
                 nis++;
                 if (c == NST - 1 && nch > NST) {
                     // the ring is full: the CTA's later row groups into L2, 64 KB per request
-                    const uint8_t* a = p.codes + (size_t)r0 * kb;
                     const size_t total = (size_t)R * kb;
-                    for (size_t o = (size_t)(NST / nkc) * TGB * 16 * kb; o < total; o += 65536) {
-                        const uint32_t bytes = (uint32_t)(total - o < 65536 ? total - o : 65536);
-                        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a + o), "r"(bytes) : "memory");
+                    for (int w = 0; w < NW; w++) {
+                        const uint8_t* a = (w ? p.codes2 : p.codes) + (size_t)r0 * kb;
+                        for (size_t o = (size_t)(NST / nkc) * TGB * 16 * kb; o < total; o += 65536) {
+                            const uint32_t bytes = (uint32_t)(total - o < 65536 ? total - o : 65536);
+                            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a + o), "r"(bytes) : "memory");
+                        }
                     }
                 }
                 cur.next(NST, nkc);
@@ -366,20 +394,22 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
     }
     consumer_sync();
 
-    // ---- main loop.  Warp w works on tile pair w / wpp of every row group (two MMA chains)
-    // and on pack blocks part, part + wpp, ... (part = w % wpp) of every chunk, so its running
-    // sums stay in registers over the whole K range.  A wait that gives up marks the status
-    // and the remaining waits are skipped; the loop still runs to its end.
+    // ---- main loop.  Warp w works on tile pair w / wpp of every row group (two MMA chains:
+    // tiles 2 pair and 2 pair + 1, or in the dual form gate tile pair and up tile pair) and on
+    // pack blocks part, part + wpp, ... (part = w % wpp) of every chunk, so its running sums
+    // stay in registers over the whole K range.  A wait that gives up marks the status and
+    // the remaining waits are skipped; the loop still runs to its end.
     bool failed = !warp_wait(sbar, 0);
     const int gsh = __ffs(p.group) - 1 - 7;  // group = 128 << gsh
     const uint16_t* srow = reinterpret_cast<const uint16_t*>(scal + ((int64_t)r0 * G * 2 - s_lo));
     const int tlast = TC - (ngrp - 1) * TGB;  // tiles of the last row group
-    const int np = (TGB + 1) >> 1;           // tile pairs per row group
-    const int wpp = np <= 2 ? HM_MAX_PARTS : HM_CWARPS / 4;  // warps per pair (a power of two)
+    const int wpp = hm_parts(TGB, NW);  // warps per tile pair (a power of two)
     const int pair = warp / wpp, part = warp - pair * wpp;
     const int nbw = 8 / wpp > 0 ? 8 / wpp : 1;  // pack blocks per chunk and warp
     const int jb = min(g, M - 1);  // activation row of the lane's B fragments (columns >= M are never stored)
-    const size_t pstride = (size_t)16 * p.tmax * M;  // one part's partial sums
+    const size_t pstride = (size_t)16 * p.tmax * M;  // one part's (and weight's) partial sums
+    // second tile of a pair: the next tile of the box, or the same tile of the up weight
+    const uint32_t q1_off = DUAL ? 2 * box_bytes : HM_BOX;
     float tot[HM_TG][4];
 #pragma unroll
     for (int q = 0; q < HM_TG; q++) tot[q][0] = tot[q][1] = tot[q][2] = tot[q][3] = 0.f;
@@ -387,10 +417,12 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
     for (int c = 0; c < nch; c++) {
         if (!failed && !warp_wait(&full[ch.s], ch.ph)) failed = true;
         const int ntg = ch.gi == ngrp - 1 ? tlast : TGB;
-        const int ntp = min(HM_TG, ntg - HM_TG * pair);  // tiles of this warp's pair (<= 0: none)
-        const int tile0 = ch.gi * TGB + HM_TG * pair;    // its first tile in the CTA
+        // tiles of this warp's pair (<= 0: none) and its first tile in the CTA
+        const int ntp = DUAL ? (pair < ntg ? 2 : 0) : min(HM_TG, ntg - HM_TG * pair);
+        const int tile0 = ch.gi * TGB + (DUAL ? pair : HM_TG * pair);
         if (ntp > 0 && part < 8) {
-            const uint8_t* sbase = ring + (size_t)ch.s * stage_bytes + (size_t)HM_TG * pair * HM_BOX + g * 128 + ((t & 1) << 3);
+            const uint8_t* sbase = ring + (size_t)ch.s * stage_bytes + (size_t)(tile0 - ch.gi * TGB) * HM_BOX +
+                                   g * 128 + ((t & 1) << 3);
             for (int bi = 0; bi < nbw; bi++) {
                 const int blk = part + bi * wpp;  // pack block within the chunk, 0..7
                 const int pb = ch.kc * 8 + blk;
@@ -403,8 +435,8 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
                 w8[0] = *reinterpret_cast<const uint2*>(cb + 8 * 128);
                 w[1] = w8[1] = make_uint2(0u, 0u);
                 if (ntp == 2) {
-                    w[1] = *reinterpret_cast<const uint2*>(cb + HM_BOX);
-                    w8[1] = *reinterpret_cast<const uint2*>(cb + HM_BOX + 8 * 128);
+                    w[1] = *reinterpret_cast<const uint2*>(cb + q1_off);
+                    w8[1] = *reinterpret_cast<const uint2*>(cb + q1_off + 8 * 128);
                 }
                 uint32_t b[16];
                 const uint4* bp = reinterpret_cast<const uint4*>(btab + (((size_t)pb * 4 * M + jb) * 4 + t) * 16);
@@ -422,11 +454,13 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
                 if (ntp == 2) hm_tiles<2>(ac, w, w8, b);
                 else hm_tiles<1>(ac, w, w8, b);
                 const uint16_t* sg = srow + (size_t)(tile0 * 16 + g) * G + (pb >> gsh);
+                // the second tile's scales: 16 rows on, or the up weight's rows
+                const size_t q1_s = DUAL ? L.scal_w / 2 : (size_t)16 * G;
 #pragma unroll
                 for (int q = 0; q < HM_TG; q++) {
                     if (q >= ntp) continue;  // a one-tile pair: the second tile's scales do not exist
-                    const float d0 = bf16_bits_to_f32(sg[(size_t)q * 16 * G]);
-                    const float d8 = bf16_bits_to_f32(sg[((size_t)q * 16 + 8) * G]);
+                    const float d0 = bf16_bits_to_f32(sg[q * q1_s]);
+                    const float d8 = bf16_bits_to_f32(sg[q * q1_s + (size_t)8 * G]);
                     tot[q][0] = fmaf(d0, ac[q][0], tot[q][0]);
                     tot[q][1] = fmaf(d0, ac[q][1], tot[q][1]);
                     tot[q][2] = fmaf(d8, ac[q][2], tot[q][2]);
@@ -439,11 +473,12 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
         if (ch.kc == nkc - 1) {
             // end of a row group: the warp's sums for its pair's rows into its part's slots
             if (ntp > 0 && part < 8) {
-                float* sl = slot + (size_t)part * pstride;
+                float* sl = slot + (size_t)part * NW * pstride;
 #pragma unroll
                 for (int q = 0; q < HM_TG; q++) {
                     if (q >= ntp) continue;
-                    float* s0 = sl + (size_t)((tile0 + q) * 16 + g) * M;
+                    // slots [part][weight][row][m]: the dual form's second tile is the up weight's
+                    float* s0 = sl + (DUAL ? q * pstride + (size_t)(tile0 * 16 + g) * M : (size_t)((tile0 + q) * 16 + g) * M);
                     float* s8 = s0 + 8 * M;
                     if (2 * t < M) {
                         s0[2 * t] = tot[q][0];
@@ -463,14 +498,26 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
     if (failed && lane == 0) atomicOr(&g_hm_status, 1u);
     consumer_sync();
 
-    // ---- the parts' partial sums, added in a fixed order, stored as BF16
+    // ---- the parts' partial sums, added in a fixed order, stored as BF16 (the dual form: u,
+    // and h = BF16(SiLU(BF16(g)) * BF16(u)), the arithmetic of the separate gate and up launches)
     for (int o = tid; o < M * R; o += NCT) {
         const int j = o / R, row = o - j * R;
-        float sum = 0.f;
-        for (int pp = 0; pp < wpp; pp++) sum += slot[pp * pstride + (size_t)row * M + j];
+        float sum = 0.f, sum2 = 0.f;
+        for (int pp = 0; pp < wpp; pp++) {
+            sum += slot[pp * NW * pstride + (size_t)row * M + j];
+            if (DUAL) sum2 += slot[(pp * NW + 1) * pstride + (size_t)row * M + j];
+        }
         const __nv_bfloat16 bv = __float2bfloat16_rn(sum * rowback[j]);
         const uint16_t ub = *reinterpret_cast<const uint16_t*>(&bv);
         const size_t idx = (size_t)j * n + r0 + row;
+        if (DUAL) {
+            const __nv_bfloat16 uv = __float2bfloat16_rn(sum2 * rowback[j]);
+            const uint16_t uu = *reinterpret_cast<const uint16_t*>(&uv);
+            p.y2[idx] = uu;
+            const __nv_bfloat16 hb = __float2bfloat16_rn(silu_mul1(bf16_bits_to_f32(ub), bf16_bits_to_f32(uu)));
+            p.y[idx] = *reinterpret_cast<const uint16_t*>(&hb);
+            continue;
+        }
         p.y[idx] = ub;
         if (p.hgate) {
             const __nv_bfloat16 hb = __float2bfloat16_rn(silu_mul1(bf16_bits_to_f32(p.hgate[idx]), bf16_bits_to_f32(ub)));
@@ -484,25 +531,29 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
 // tiles as balance the CTA's tiles over the fewest groups of at most eight (TMA requests
 // stream faster the larger they are: a box of 8 tiles is 16 KB); the ring gets as many
 // stages as one SM holds, up to one per chunk, so a CTA's whole slice is usually requested
-// at once.
-static int hm_plan(int m, int n, int k, int group, int sms, HmParams* prm, size_t* smem_out) {
+// at once.  nw = 2: the dual (gate and up) form.
+static int hm_plan(int m, int n, int k, int group, int nw, int sms, HmParams* prm, size_t* smem_out) {
     const int ntiles = (n + 15) / 16;
     const int ncta = ntiles < sms ? ntiles : sms;
     const int tmax = (ntiles + ncta - 1) / ncta;
     const int nkc = (k / 128 + 7) / 8;
-    const int ngrp = (tmax + HM_MAX_TGB - 1) / HM_MAX_TGB;
-    const int tgb = (tmax + ngrp - 1) / ngrp;
+    // the fewest row groups whose two-stage ring fits, then as many stages as fit
+    int ngrp = (tmax + HM_MAX_TGB - 1) / HM_MAX_TGB, tgb = (tmax + ngrp - 1) / ngrp;
+    while (tgb > 1 && HmLayout(m, k, group, tgb, 2, tmax, nw).total > (size_t)HM_SMEM_LIMIT) {
+        ngrp++;
+        tgb = (tmax + ngrp - 1) / ngrp;
+    }
     const int nch = ngrp * nkc;
     int NST = HM_MAX_STAGES < nch ? HM_MAX_STAGES : nch;
     if (NST < 2) NST = 2;
-    while (NST > 2 && HmLayout(m, k, group, tgb, NST, tmax).total > (size_t)HM_SMEM_LIMIT) NST--;
+    while (NST > 2 && HmLayout(m, k, group, tgb, NST, tmax, nw).total > (size_t)HM_SMEM_LIMIT) NST--;
     prm->n = n;
     prm->k = k;
     prm->group = group;
     prm->tmax = tmax;
     prm->tgb = tgb;
     prm->nstages = NST;
-    *smem_out = HmLayout(m, k, group, tgb, NST, tmax).total;
+    *smem_out = HmLayout(m, k, group, tgb, NST, tmax, nw).total;
     return ncta;
 }
 
@@ -511,50 +562,69 @@ bool gemv_hm_supported(const bq_q2_weight* w, uint32_t m) {
     if (w->k == 0 || w->n == 0 || m < 1 || m > 8) return false;
     HmParams prm;
     size_t smem = 0;
-    hm_plan((int)m, (int)w->n, (int)w->k, (int)w->group, sm_count(), &prm, &smem);
+    hm_plan((int)m, (int)w->n, (int)w->k, (int)w->group, 1, sm_count(), &prm, &smem);
     return smem <= (size_t)HM_SMEM_LIMIT;
 }
 
-typedef void (*HmKernel)(const CUtensorMap, const HmParams);
+// The dual form for an FFN's gate and up weights (the caller has checked that they match).
+bool gemv_hm_dual_supported(const bq_q2_weight* gate, uint32_t m) {
+    if (gate->k == 0 || gate->n == 0 || m < 1 || m > 8) return false;
+    HmParams prm;
+    size_t smem = 0;
+    hm_plan((int)m, (int)gate->n, (int)gate->k, (int)gate->group, 2, sm_count(), &prm, &smem);
+    return smem <= (size_t)HM_SMEM_LIMIT;
+}
 
+typedef void (*HmKernel)(const CUtensorMap, const CUtensorMap, const HmParams);
+
+template <bool DUAL>
 static HmKernel hm_kernel_for(uint32_t m) {
     switch (m) {
-        case 1: return q2_gemv_hm_kernel<1>;
-        case 2: return q2_gemv_hm_kernel<2>;
-        case 3: return q2_gemv_hm_kernel<3>;
-        case 4: return q2_gemv_hm_kernel<4>;
-        case 5: return q2_gemv_hm_kernel<5>;
-        case 6: return q2_gemv_hm_kernel<6>;
-        case 7: return q2_gemv_hm_kernel<7>;
-        case 8: return q2_gemv_hm_kernel<8>;
+        case 1: return q2_gemv_hm_kernel<1, DUAL>;
+        case 2: return q2_gemv_hm_kernel<2, DUAL>;
+        case 3: return q2_gemv_hm_kernel<3, DUAL>;
+        case 4: return q2_gemv_hm_kernel<4, DUAL>;
+        case 5: return q2_gemv_hm_kernel<5, DUAL>;
+        case 6: return q2_gemv_hm_kernel<6, DUAL>;
+        case 7: return q2_gemv_hm_kernel<7, DUAL>;
+        case 8: return q2_gemv_hm_kernel<8, DUAL>;
         default: return nullptr;
     }
 }
 
-int launch_q2_gemv_hm(const uint16_t* x, const bq_q2_weight* w, uint16_t* y, uint32_t m, uint16_t* hgate,
-                      cudaStream_t stream, const char* who) {
-    static int configured_smem[64][8] = {};
+// Shared launch path: w2 / y2 non-null selects the dual form (w = gate, w2 = up; y gets h,
+// y2 gets u).
+static int launch_hm(const uint16_t* x, const bq_q2_weight* w, const bq_q2_weight* w2, uint16_t* y, uint16_t* y2,
+                     uint32_t m, uint16_t* hgate, cudaStream_t stream, const char* who) {
+    static int configured_smem[64][2][8] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 64) dev = 63;
     if (m < 1 || m > 8) return fail(BQ_ERR_INVALID, "%s: m = %u, must be 1..8", who, m);
+    const bool dual = w2 != nullptr;
     HmParams prm;
     size_t smem = 0;
-    const int ncta = hm_plan((int)m, (int)w->n, (int)w->k, (int)w->group, sm_count(), &prm, &smem);
+    const int ncta = hm_plan((int)m, (int)w->n, (int)w->k, (int)w->group, dual ? 2 : 1, sm_count(), &prm, &smem);
     if (smem > (size_t)HM_SMEM_LIMIT) return fail(BQ_ERR_INVALID, "%s: shape needs too much shared memory", who);
-    const HmKernel kern = hm_kernel_for(m);
-    if ((size_t)configured_smem[dev][m - 1] < smem) {
+    const HmKernel kern = dual ? hm_kernel_for<true>(m) : hm_kernel_for<false>(m);
+    if ((size_t)configured_smem[dev][dual][m - 1] < smem) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return fail(BQ_ERR_LAUNCH, "%s: cannot reserve %zu bytes of shared memory", who, smem);
-        configured_smem[dev][m - 1] = (int)smem;
+        configured_smem[dev][dual][m - 1] = (int)smem;
     }
-    CUtensorMap tmap;
+    CUtensorMap tmap, tmap2;
     int st = cached_tmap_2d_u8(&tmap, w->data, w->k / 4, w->n, w->k / 4, 128, 16 * prm.tgb, true, who);
     if (st) return st;
+    tmap2 = tmap;
+    if (dual && (st = cached_tmap_2d_u8(&tmap2, w2->data, w2->k / 4, w2->n, w2->k / 4, 128, 16 * prm.tgb, true, who)))
+        return st;
     prm.codes = (const uint8_t*)w->data;
     prm.scales = (const uint16_t*)((const uint8_t*)w->data + (size_t)w->n * (w->k / 4));
+    prm.codes2 = dual ? (const uint8_t*)w2->data : nullptr;
+    prm.scales2 = dual ? (const uint16_t*)((const uint8_t*)w2->data + (size_t)w2->n * (w2->k / 4)) : nullptr;
     prm.x = x;
     prm.y = y;
+    prm.y2 = y2;
     prm.hgate = hgate;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ncta);
@@ -566,8 +636,18 @@ int launch_q2_gemv_hm(const uint16_t* x, const bq_q2_weight* w, uint16_t* y, uin
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, tmap, prm) != cudaSuccess) return check_launch(who);
+    if (cudaLaunchKernelEx(&cfg, kern, tmap, tmap2, prm) != cudaSuccess) return check_launch(who);
     return check_launch(who);
+}
+
+int launch_q2_gemv_hm(const uint16_t* x, const bq_q2_weight* w, uint16_t* y, uint32_t m, uint16_t* hgate,
+                      cudaStream_t stream, const char* who) {
+    return launch_hm(x, w, nullptr, y, nullptr, m, hgate, stream, who);
+}
+
+int launch_q2_gemv_hm_dual(const uint16_t* x, const bq_q2_weight* gate, const bq_q2_weight* up, uint16_t* h,
+                           uint16_t* u, uint32_t m, cudaStream_t stream, const char* who) {
+    return launch_hm(x, gate, up, h, u, m, nullptr, stream, who);
 }
 
 }  // namespace bq8

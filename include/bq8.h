@@ -119,8 +119,10 @@ int silu_mul_bf16(const uint16_t* gate, const uint16_t* up, uint16_t* out, size_
  *   gate_scratch = SiLU(gate_scratch) * up_scratch; out = gate_scratch @ down^T ([m][hidden]).
  * Shapes: gate, up: n = inter, k = hidden; down: n = hidden, k = inter.  On return (after
  * the stream drains) gate_scratch holds h and up_scratch holds u, as on the page; the two
- * must not overlap (BQ_ERR_INVALID).  Three launches: the SiLU*mul step runs in the up
- * projection's epilogue with the same arithmetic as silu_mul_bf16.
+ * must not overlap (BQ_ERR_INVALID).  Two launches: one streams the gate and up weights
+ * together and forms u and h (the SiLU*mul with the same arithmetic as silu_mul_bf16 on
+ * the BF16 g and u), then the down projection; where the two weights' tile pairs do not fit
+ * one SM (large k at m near 8) the gate and up projections run as two launches instead.
  * Source: dense_ffn_decode_batch.rs, `forward_km_q2`. */
 int ffn_q2_km(const uint16_t* x, const bq_q2_weight* gate, const bq_q2_weight* up, const bq_q2_weight* down,
               uint16_t* gate_scratch, uint16_t* up_scratch, uint16_t* out, uint32_t m, bq_stream_t stream);
