@@ -456,6 +456,7 @@ def _rows_prefill(rows, reps, dev, hbm_peak, bf16_peak):
         qb = m * k * 2 + B.q8_1_bytes(m, k)
         tm = _time_calls(lambda i: B.q2_mmq_gemm(act, w, m, out=out), max(3, reps // 5))
         tg = _time_calls(lambda i: torch.matmul(x, wd.t(), out=out), max(3, reps // 5))
+        to = _time_calls(lambda i: B.dense_gemm_bf16(x, wd, out=out), max(3, reps // 5))
         flops = 2.0 * m * n * k
         rows["a5_q8_1_m%d" % m] = {"us": tq * 1e6, "GBps": qb / tq / 1e9, "frac_hbm": qb / tq / 1e9 / hbm_peak}
         rows["a6_q2_mmq_m%d" % m] = {"us": tm * 1e6, "TOPS": flops / tm / 1e12,
@@ -464,8 +465,13 @@ def _rows_prefill(rows, reps, dev, hbm_peak, bf16_peak):
                                      "pipe": "tcgen05.mma kind::f16 M128 N256 K16: exact BF16 weights d(c-2), q8_1 "
                                              "activations as a hi/lo BF16 pair (2 MMAs per K16; sm_103a has no "
                                              "tcgen05 int8)"}
+        rows["a9_dequant_plus_gemm_m%d" % m] = {"us": (to + rows["a8_dequant_16384x5120"]["us"] / 1e6) * 1e6,
+                                               "gemm_us": to * 1e6, "TFLOPS_gemm": flops / to / 1e12,
+                                               "frac_bf16_dense_peak": flops / to / 1e12 / bf16_peak,
+                                               "gemm": "dense_gemm_bf16 (this library's tcgen05 kernel)"}
         rows["a9_dequant_plus_cublas_m%d" % m] = {"us": (tg + rows["a8_dequant_16384x5120"]["us"] / 1e6) * 1e6,
-                                                 "gemm_us": tg * 1e6, "TFLOPS_gemm": flops / tg / 1e12}
+                                                 "gemm_us": tg * 1e6, "TFLOPS_gemm": flops / tg / 1e12,
+                                                 "gemm": "cuBLAS through torch.matmul (comparison only)"}
         del x, act, out
     del w, wd
     torch.cuda.empty_cache()

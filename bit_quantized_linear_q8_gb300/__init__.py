@@ -17,7 +17,8 @@ from ._abi import BQ8Error, LibraryNotBuilt, check, lib  # noqa: F401
 
 __all__ = [
     "Q2Weight", "q2_pack", "quantize_weight_q4k", "quantize_act_q8_1", "q2_gemv", "q2_gemv_batchm",
-    "silu_mul_bf16", "ffn_q2_km", "ffn_q2_km_noalloc", "q2_mmq_gemm", "q4k_mmq_gemm", "dequant_q2_to_bf16", "q2_prefill_proj",
+    "silu_mul_bf16", "ffn_q2_km", "ffn_q2_km_noalloc", "q2_mmq_gemm", "q4k_mmq_gemm", "dequant_q2_to_bf16",
+    "dense_gemm_bf16", "dequant_nvfp4_to_bf16", "q2_prefill_proj",
     "q2_weight_bytes", "q8_1_bytes", "q4k_weight_bytes", "BQ8Error", "LibraryNotBuilt",
 ]
 
@@ -50,6 +51,14 @@ def _need(t, dtype, name, shape=None):
     return t
 
 
+def _need_bytes(t, nbytes, name):
+    """A uint8 CUDA buffer of at least `nbytes` bytes."""
+    _need(t, _torch().uint8, name)
+    if t.numel() < nbytes:
+        raise ValueError("%s holds %d bytes, needs %d" % (name, t.numel(), nbytes))
+    return t
+
+
 def q2_weight_bytes(n: int, k: int, group: int = 128) -> int:
     return int(lib().bq_q2_weight_bytes(n, k, group))
 
@@ -71,6 +80,7 @@ class Q2Weight:
     group: int = 128
 
     def desc(self):
+        _need_bytes(self.data, q2_weight_bytes(self.n, self.k, self.group), "Q2Weight.data")
         return _abi.Q2WeightDesc(self.data.data_ptr(), self.n, self.k, self.group)
 
 
@@ -102,6 +112,7 @@ def quantize_act_q8_1(x, out=None):
     _need(x, torch.bfloat16, "x")
     if out is None:
         out = torch.empty(q8_1_bytes(m, k), dtype=torch.uint8, device=x.device)
+    _need_bytes(out, q8_1_bytes(m, k), "out")
     check(lib().quantize_act_q8_1(_ptr(x), _ptr(out), m, k, _stream()))
     return out
 
@@ -112,6 +123,7 @@ def q2_gemv(x, w: Q2Weight, out=None):
     _need(x, torch.bfloat16, "x", (1, w.k))
     if out is None:
         out = torch.empty((1, w.n), dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, "out", (1, w.n))
     d = w.desc()
     check(lib().q2_gemv(_ptr(x), ctypes.byref(d), _ptr(out), _stream()))
     return out
@@ -124,6 +136,7 @@ def q2_gemv_batchm(x, w: Q2Weight, out=None):
     _need(x, torch.bfloat16, "x", (m, w.k))
     if out is None:
         out = torch.empty((m, w.n), dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, "out", (m, w.n))
     d = w.desc()
     check(lib().q2_gemv_batchm(_ptr(x), ctypes.byref(d), _ptr(out), m, _stream()))
     return out
@@ -135,6 +148,7 @@ def silu_mul_bf16(gate, up, out=None):
     _need(up, torch.bfloat16, "up", tuple(gate.shape))
     if out is None:
         out = torch.empty_like(gate)
+    _need(out, torch.bfloat16, "out", tuple(gate.shape))
     check(lib().silu_mul_bf16(_ptr(gate), _ptr(up), _ptr(out), gate.numel(), _stream()))
     return out
 
@@ -151,6 +165,9 @@ def ffn_q2_km(x, gate: Q2Weight, up: Q2Weight, down: Q2Weight, gate_scratch=None
         up_scratch = torch.empty((m, inter), dtype=torch.bfloat16, device=x.device)
     if out is None:
         out = torch.empty((m, hidden), dtype=torch.bfloat16, device=x.device)
+    _need(gate_scratch, torch.bfloat16, "gate_scratch", (m, inter))
+    _need(up_scratch, torch.bfloat16, "up_scratch", (m, inter))
+    _need(out, torch.bfloat16, "out", (m, down.n))
     dg, du, dd = gate.desc(), up.desc(), down.desc()
     check(lib().ffn_q2_km(_ptr(x), ctypes.byref(dg), ctypes.byref(du), ctypes.byref(dd), _ptr(gate_scratch),
                           _ptr(up_scratch), _ptr(out), m, _stream()))
@@ -176,9 +193,10 @@ def ffn_q2_km_noalloc(x, gate: Q2Weight, up: Q2Weight, down: Q2Weight, out=None)
 def q2_mmq_gemm(act_q8, w: Q2Weight, m: int, out=None):
     """q8_1 activations for [m, w.k] -> out [m, n] bf16 (group must be 128)."""
     torch = _torch()
-    _need(act_q8, torch.uint8, "act_q8")
+    _need_bytes(act_q8, q8_1_bytes(m, w.k), "act_q8")
     if out is None:
         out = torch.empty((m, w.n), dtype=torch.bfloat16, device=act_q8.device)
+    _need(out, torch.bfloat16, "out", (m, w.n))
     d = w.desc()
     check(lib().q2_mmq_gemm(_ptr(act_q8), ctypes.byref(d), _ptr(out), m, _stream()))
     return out
@@ -186,10 +204,11 @@ def q2_mmq_gemm(act_q8, w: Q2Weight, m: int, out=None):
 
 def q4k_mmq_gemm(act_q8, w_q4k, m: int, n: int, k: int, out=None):
     torch = _torch()
-    _need(act_q8, torch.uint8, "act_q8")
-    _need(w_q4k, torch.uint8, "w_q4k")
+    _need_bytes(act_q8, q8_1_bytes(m, k), "act_q8")
+    _need_bytes(w_q4k, q4k_weight_bytes(n, k), "w_q4k")
     if out is None:
         out = torch.empty((m, n), dtype=torch.bfloat16, device=act_q8.device)
+    _need(out, torch.bfloat16, "out", (m, n))
     check(lib().q4k_mmq_gemm(_ptr(act_q8), _ptr(w_q4k), _ptr(out), m, n, k, _stream()))
     return out
 
@@ -198,8 +217,24 @@ def dequant_q2_to_bf16(w: Q2Weight, out=None):
     torch = _torch()
     if out is None:
         out = torch.empty((w.n, w.k), dtype=torch.bfloat16, device=w.data.device)
+    _need(out, torch.bfloat16, "out", (w.n, w.k))
     d = w.desc()
     check(lib().dequant_q2_to_bf16(ctypes.byref(d), _ptr(out), _stream()))
+    return out
+
+
+def dense_gemm_bf16(a, w, out=None):
+    """out [m, n] = a [m, k] @ w [n, k]^T, BF16 in and out, fp32 accumulation (the fallback
+    route's dense GEMM, init_q2.rs `dense_gemm_bf16_pipelined`); k a multiple of 64."""
+    torch = _torch()
+    m, k = a.shape
+    n = w.shape[0]
+    _need(a, torch.bfloat16, "a", (m, k))
+    _need(w, torch.bfloat16, "w", (n, k))
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
+    _need(out, torch.bfloat16, "out", (m, n))
+    check(lib().dense_gemm_bf16(_ptr(a), _ptr(w), _ptr(out), m, n, k, _stream()))
     return out
 
 
@@ -213,24 +248,26 @@ def dequant_nvfp4_to_bf16(packed, scales, scale2: float, n: int, k: int, out=Non
         raise ValueError("packed must hold n*k/2 bytes and scales n*k/16 bytes")
     if out is None:
         out = torch.empty((n, k), dtype=torch.bfloat16, device=packed.device)
+    _need(out, torch.bfloat16, "out", (n, k))
     check(lib().dequant_nvfp4_to_bf16(_ptr(packed), _ptr(scales), _ptr(out), ctypes.c_float(scale2), n, k,
                                       _stream()))
     return out
 
 
-def q2_prefill_proj(x, w: Q2Weight, mode: str = "mmq", act_q8=None, scratch=None):
+def q2_prefill_proj(x, w: Q2Weight, mode: str = "mmq", act_q8=None, scratch=None, out=None):
     """The prefill projection out = x @ W^T by either route of init_q2.rs
     `qkvz_q2_prefill_gemm`: "mmq" (q8_1 quantisation + Q2 MMQ, group 128 only) or
-    "dequant" (dequantise to BF16 into `scratch`, then a dense BF16 GEMM -- a plain library
-    GEMM, cuBLAS through torch.matmul).  Returns (out, mode_used)."""
+    "dequant" (dequantise to BF16 into `scratch` [n, k], then this library's tcgen05 BF16
+    GEMM).  Returns (out, mode_used)."""
     torch = _torch()
     m = x.shape[0]
     if mode == "mmq":
         if w.group != 128:
             raise ValueError("the MMQ route needs group size 128")
         act_q8 = quantize_act_q8_1(x, out=act_q8)
-        return q2_mmq_gemm(act_q8, w, m), "mmq"
+        return q2_mmq_gemm(act_q8, w, m, out=out), "mmq"
     if mode == "dequant":
+        _need(x, torch.bfloat16, "x", (m, w.k))
         wd = dequant_q2_to_bf16(w, out=scratch)
-        return torch.matmul(x, wd.t()), "dequant"
+        return dense_gemm_bf16(x, wd, out=out), "dequant"
     raise ValueError("mode must be 'mmq' or 'dequant'")

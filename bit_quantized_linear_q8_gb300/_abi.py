@@ -41,6 +41,7 @@ SIGNATURES = {
     "q2_mmq_gemm": (I, [P, WD, P, U32, P]),
     "q4k_mmq_gemm": (I, [P, P, P, U32, U32, U32, P]),
     "dequant_q2_to_bf16": (I, [WD, P, P]),
+    "dense_gemm_bf16": (I, [P, P, P, U32, U32, U32, P]),
     "dequant_nvfp4_to_bf16": (I, [P, P, P, ctypes.c_float, U32, U32, P]),
     "bq_device_status": (I, []),
     "bq_last_error": (ctypes.c_char_p, []),

@@ -166,7 +166,8 @@ int make_tmap_3d_u8(CUtensorMap* map, const void* base, const uint64_t (&dims)[3
 extern "C" {
 
 int bq_device_status(void) {
-    const unsigned int s = bq8::gemv_status_take() | bq8::gemv_hm_status_take() | bq8::mmq_tc_status_take();
+    const unsigned int s = bq8::gemv_status_take() | bq8::gemv_hm_status_take() | bq8::mmq_tc_status_take() |
+                           bq8::gemm_bf16_status_take();
     if (s) return bq8::fail(BQ_ERR_DEVICE, "a kernel gave up on a bounded wait (status bits 0x%x)", s);
     return bq8::ok();
 }

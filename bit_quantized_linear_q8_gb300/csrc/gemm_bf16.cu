@@ -1,0 +1,271 @@
+// gemm_bf16.cu -- dense BF16 GEMM on the tcgen05 tensor cores: out[m, n] = a[m, k] @ w[n, k]^T.
+//
+// Source: init_q2.rs `qkvz_q2_prefill_gemm`, the fallback branch: `dequant_q2_0_gn_to_bf16`
+// writes the weight as BF16 and `dense_gemm_bf16_pipelined` multiplies it with the BF16
+// activations (fp32 accumulation, BF16 store).
+//
+// Design (GB300, sm_103a).  A plain tiled GEMM on the fifth-generation tensor cores:
+//  * Tile 128 (m) x 256 (n), K step 64.  Both operands are K-major BF16 in global memory and
+//    arrive by TMA with the 128-byte swizzle (a box row is 64 values = 128 bytes), four
+//    stages of 16 KB (a) + 32 KB (w) in shared memory; the MMAs read them through
+//    shared-memory descriptors (swizzle 128B, 8-row groups 1024 bytes apart, each K16 slice
+//    32 bytes further into the swizzle atom).
+//  * The accumulator (128 lanes x 256 fp32 columns) lives in tensor memory.
+//  * Warp 1 (one lane) streams the tiles; warp 0 allocates tensor memory and one lane issues
+//    the M128 N256 K16 MMAs (four per K step), committing each step to the stage's `empty`
+//    barrier and the last one to `done`; warps 4-7 (one tensor-memory lane quadrant each,
+//    one output row per thread) read the accumulator with tcgen05.ld and store BF16.
+//  * Grid: one CTA per output tile, m tiles varying fastest.
+//  * Every wait is bounded; a wait that gives up raises the CTA's abort flag and the status
+//    word, and the kernel winds down (the MMA warp still waits for its own MMAs before the
+//    tensor memory is freed).
+#include "common.cuh"
+
+namespace bq8 {
+
+static __device__ unsigned int g_gemm_status;
+
+unsigned int gemm_bf16_status_take() {
+    unsigned int v = 0, zero = 0;
+    cudaDeviceSynchronize();
+    cudaMemcpyFromSymbol(&v, g_gemm_status, sizeof v);
+    cudaMemcpyToSymbol(g_gemm_status, &zero, sizeof zero);
+    return v;
+}
+
+constexpr int GB_BM = 128;
+constexpr int GB_BN = 256;
+constexpr int GB_BK = 64;
+constexpr int GB_NS = 4;                               // pipeline stages
+constexpr uint32_t GB_ASTAGE = GB_BM * GB_BK * 2;      // 16 KB
+constexpr uint32_t GB_BSTAGE = GB_BN * GB_BK * 2;      // 32 KB
+constexpr uint32_t GB_STAGE = GB_ASTAGE + GB_BSTAGE;
+constexpr int GB_THREADS = 8 * 32;
+constexpr uint32_t GB_TMEM_COLS = 256;
+constexpr uint32_t GB_WAIT_LIMIT = 1u << 20;           // try_waits before a wait gives up
+constexpr size_t GB_SMEM = 1024 + (size_t)GB_NS * GB_STAGE + (2 * GB_NS + 1) * 8 + 16;
+static_assert(GB_SMEM <= 227 * 1024, "shared memory budget");
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bit 4), A and B BF16 (bits 7-9,
+// 10-12), both K-major (bits 15, 16 clear), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t GB_IDESC =
+    (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(GB_BN >> 3) << 17) | ((uint32_t)(GB_BM >> 4) << 24);
+
+// Shared-memory matrix descriptor for a K-major tile with the 128-byte swizzle: start address,
+// leading byte offset 16 (unused by this layout), stride byte offset 1024 (one 8-row group of
+// 128-byte rows), descriptor version bit 46, swizzle mode 2 (128 bytes) at bits 61-63.
+__device__ __forceinline__ uint64_t gb_desc(uint32_t addr) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+           (2ull << 61);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, M128 N256 K16, BF16 in, fp32 accumulate.
+__device__ __forceinline__ void gb_mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.u32 p, %3, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %4, p;\n}\n" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(accumulate), "r"(GB_IDESC));
+}
+
+__device__ __forceinline__ void gb_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ bool gb_try(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Bounded wait that also gives up as soon as another thread of the CTA has raised `abort`.
+__device__ __forceinline__ bool gb_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    for (uint32_t it = 0; it < GB_WAIT_LIMIT; it++) {
+        if (gb_try(bar, parity)) return true;
+        if (*abort) return false;
+    }
+    *abort = 1;
+    atomicOr(&g_gemm_status, 1u);
+    return false;
+}
+
+__device__ __forceinline__ void gb_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// (Launch bounds of 256 threads: eight warps, two per SM sub-partition.)
+__global__ void __launch_bounds__(GB_THREADS, 1)
+    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapW,
+                        uint16_t* __restrict__ out, int m, int n, int k, int ntm) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* stages = align1024(smem_raw);  // [stage][a 128 x 64 | w 256 x 64] BF16, 128-byte swizzle
+    uint64_t* full = reinterpret_cast<uint64_t*>(stages + GB_NS * GB_STAGE);
+    uint64_t* empty = full + GB_NS;
+    uint64_t* done = empty + GB_NS;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // m tiles vary fastest: the CTAs resident at once share few weight tiles, and the
+    // activations (m x k) stay in L2 while each weight tile is read once
+    const int m0 = (blockIdx.x % ntm) * GB_BM, n0 = (blockIdx.x / ntm) * GB_BN;
+    const int S = k / GB_BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < GB_NS; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(done, 1);
+        *abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                     "n"(GB_TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tbase = *tslot;
+
+    if (warp == 1) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int s = 0; s < S; s++) {
+                const int st = s % GB_NS;
+                if (s >= GB_NS && !gb_wait(&empty[st], (uint32_t)((s / GB_NS) - 1) & 1u, abort)) break;
+                uint8_t* dst = stages + (size_t)st * GB_STAGE;
+                mbar_arrive_expect_tx(&full[st], GB_STAGE);
+                tma_load_2d(dst, &mapA, s * GB_BK * 2, m0, &full[st]);
+                tma_load_2d(dst + GB_ASTAGE, &mapW, s * GB_BK * 2, n0, &full[st]);
+                issued++;
+            }
+            // wind down: every copy requested must have landed before the CTA exits
+            for (int s = issued > GB_NS ? issued - GB_NS : 0; s < issued; s++)
+                if (!mbar_wait_suspend(&full[s % GB_NS], (uint32_t)(s / GB_NS) & 1u)) atomicOr(&g_gemm_status, 2u);
+        }
+        __syncwarp();
+    } else if (warp == 0) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            for (int s = 0; s < S; s++) {
+                const int st = s % GB_NS;
+                if (!gb_wait(&full[st], (uint32_t)(s / GB_NS) & 1u, abort)) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t abase = smem_u32(stages + (size_t)st * GB_STAGE);
+                const uint32_t bbase = abase + GB_ASTAGE;
+#pragma unroll
+                for (int kk = 0; kk < GB_BK / 16; kk++)
+                    gb_mma(tbase, gb_desc(abase + 32u * kk), gb_desc(bbase + 32u * kk), (s | kk) != 0);
+                gb_commit(&empty[st]);  // the stage is free once these MMAs have read it
+            }
+            gb_commit(done);  // completes once every MMA issued above has finished
+            if (!mbar_wait_suspend(done, 0)) atomicOr(&g_gemm_status, 2u);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------------- epilogue
+        // warp w reads tensor-memory lanes 32 (w % 4) .. + 31: output rows m0 + 32 (w % 4) + lane
+        const int qd = warp & 3;
+        bool ok = mbar_wait_suspend(done, 0);
+        if (!ok) atomicOr(&g_gemm_status, 2u);
+        ok = __all_sync(0xffffffffu, ok && !*abort) != 0;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const int row = m0 + 32 * qd + lane;
+        const uint32_t tq = tbase + ((uint32_t)(32 * qd) << 16);
+        const bool vec = (n & 7) == 0;
+        if (ok) {
+#pragma unroll 1
+            for (int c = 0; c < GB_BN / 32; c++) {
+                const int col0 = n0 + 32 * c;
+                if (col0 >= n) break;  // warp-uniform
+                uint32_t v[32];
+                gb_ld32(tq + 32u * c, v);
+                if (row >= m) continue;
+                uint16_t* dst = out + (size_t)row * n + col0;
+                if (vec && col0 + 32 <= n) {
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        uint4 o;
+                        o.x = bf162_bits(__floats2bfloat162_rn(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])));
+                        o.y = bf162_bits(__floats2bfloat162_rn(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])));
+                        o.z = bf162_bits(__floats2bfloat162_rn(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])));
+                        o.w = bf162_bits(__floats2bfloat162_rn(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+                        *reinterpret_cast<uint4*>(dst + 8 * q) = o;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; e++) {
+                        if (col0 + e < n) {
+                            const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(v[e]));
+                            dst[e] = *reinterpret_cast<const uint16_t*>(&b);
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "n"(GB_TMEM_COLS));
+    }
+}
+
+}  // namespace bq8
+
+using namespace bq8;
+
+extern "C" int dense_gemm_bf16(const uint16_t* a, const uint16_t* w, uint16_t* out, uint32_t m, uint32_t n,
+                               uint32_t k, bq_stream_t stream) {
+    const char* who = "dense_gemm_bf16";
+    if (m == 0 || n == 0) return ok();
+    if (k == 0) {
+        if (!out) return fail(BQ_ERR_INVALID, "%s: out is NULL", who);
+        if (cudaMemsetAsync(out, 0, (size_t)m * n * 2, (cudaStream_t)stream) != cudaSuccess)
+            return fail(BQ_ERR_LAUNCH, "%s: memset failed", who);
+        return ok();
+    }
+    if (k % GB_BK != 0) return fail(BQ_ERR_INVALID, "%s: k = %u, must be a multiple of %d", who, k, GB_BK);
+    if (m >= (1u << 30) || n >= (1u << 30) || (uint64_t)k * 2 >= (1ull << 32))
+        return fail(BQ_ERR_INVALID, "%s: shape too large", who);
+    if (!a || !w || !out || !aligned16(a) || !aligned16(w) || !aligned16(out))
+        return fail(BQ_ERR_INVALID, "%s: a, w and out must be non-NULL and 16-byte aligned", who);
+    static int configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 64) dev = 63;
+    if (!configured[dev]) {
+        if (cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GB_SMEM) !=
+            cudaSuccess)
+            return fail(BQ_ERR_LAUNCH, "%s: cannot reserve %zu bytes of shared memory", who, GB_SMEM);
+        configured[dev] = 1;
+    }
+    // both operands as byte matrices with 128-byte (64-value) box rows
+    CUtensorMap ma, mw;
+    int st = cached_tmap_2d_u8(&ma, a, (uint64_t)k * 2, m, (uint64_t)k * 2, 128, GB_BM, true, who);
+    if (st) return st;
+    if ((st = cached_tmap_2d_u8(&mw, w, (uint64_t)k * 2, n, (uint64_t)k * 2, 128, GB_BN, true, who))) return st;
+    const int ntm = (int)((m + GB_BM - 1) / GB_BM), ntn = (int)((n + GB_BN - 1) / GB_BN);
+    gemm_bf16_tc_kernel<<<(unsigned)(ntm * ntn), GB_THREADS, GB_SMEM, (cudaStream_t)stream>>>(ma, mw, out, (int)m, (int)n,
+                                                                                             (int)k, ntm);
+    return check_launch(who);
+}

@@ -173,6 +173,19 @@ int q4k_mmq_gemm(const void* act_q8, const void* w_q4k, uint16_t* out, uint32_t 
  * caller's scratch, then a dense BF16 GEMM). */
 int dequant_q2_to_bf16(const bq_q2_weight* w, uint16_t* out, bq_stream_t stream);
 
+/* Dense BF16 GEMM, the second half of the fallback prefill route: out[m, n] = a[m, k] @
+ * w[n, k]^T with fp32 accumulation and one BF16 rounding per output (round to nearest even).
+ * a: [m][k] BF16 row-major (the activations), w: [n][k] BF16 row-major (a dequantised
+ * weight, as dequant_q2_to_bf16 writes it), out: [m][n] BF16 row-major; all three device
+ * pointers, 16-byte aligned, owned by the caller.  k must be a multiple of 64 (else
+ * BQ_ERR_INVALID); m = 0 or n = 0 is a no-op, k = 0 writes zeros.  Tensor-core (tcgen05)
+ * kernel of this library, not a vendor GEMM.  A failed internal wait is reported by
+ * bq_device_status.
+ * Source: init_q2.rs, `qkvz_q2_prefill_gemm` (the fallback: `dequant_q2_0_gn_to_bf16`, then
+ * `dense_gemm_bf16_pipelined`). */
+int dense_gemm_bf16(const uint16_t* a, const uint16_t* w, uint16_t* out, uint32_t m, uint32_t n, uint32_t k,
+                    bq_stream_t stream);
+
 /* Dequantise an NVFP4 weight [n][k] to BF16 out[n][k] (the weight-preparation step before
  * quantize_weight_q4k):  w = e2m1(code) * e4m3(scale) * scale2, the exact product rounded
  * once to BF16 (round to nearest even).

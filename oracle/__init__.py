@@ -12,6 +12,7 @@ Parity status of each function (what pins it, in ``tests/test_oracle_pins.py``):
   q2_pack / q2_unpack  -- pinned by a hand-derived byte pattern and round trips
   q2_dequant_bf16      -- pinned by the four code values and numpy products
   q2_gemv / q2_mmq     -- pinned by closed forms and numpy matmul of the operands
+  gemm_bf16            -- pinned by a hand-computed product, the identity, numpy matmul
   silu_mul_bf16        -- pinned against torch's SiLU in float64
   quantize_q8_1        -- pinned by invariants (s = d*sum q), exact integer rows, ties
   quantize_q4k         -- pinned by the error bound, zero blocks, and layout round trips
@@ -52,6 +53,7 @@ def lib():
             "orc_q2_unpack": (None, [P, I, I, I, P, P]),
             "orc_q2_dequant_bf16": (None, [P, I, I, I, P]),
             "orc_q2_gemv": (None, [P, P, I, I, I, I, P]),
+            "orc_gemm_bf16": (None, [P, P, I, I, I, P]),
             "orc_silu_mul_bf16": (None, [P, P, I, P]),
             "orc_ffn_q2": (None, [P, P, P, P, I, I, I, I, P, P, P, P]),
             "orc_quantize_q8_1": (None, [P, I, I, P]),
@@ -167,6 +169,20 @@ def q2_gemv(x_bits, packed, n: int, k: int, group: int = 128):
     y = np.zeros((m, n), dtype=np.float64)
     lib().orc_q2_gemv(_p(x), _p(packed), m, n, k, group, _p(y))
     return y
+
+
+def gemm_bf16(a_bits, w_bits):
+    """Dense BF16 GEMM of the fallback prefill route (init_q2.rs `qkvz_q2_prefill_gemm`,
+    `dense_gemm_bf16_pipelined`): out [m, n] = a [m, k] @ w [n, k]^T of the BF16 values,
+    summed in fp64 (the store's BF16 rounding is left to the caller)."""
+    a = _c(a_bits, np.uint16)
+    w = _c(w_bits, np.uint16)
+    m, k = a.shape
+    n = w.shape[0]
+    assert w.shape == (n, k)
+    out = np.zeros((m, n), dtype=np.float64)
+    lib().orc_gemm_bf16(_p(a), _p(w), m, n, k, _p(out))
+    return out
 
 
 def silu_mul_bf16(gate_bits, up_bits):

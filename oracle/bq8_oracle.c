@@ -183,6 +183,20 @@ void orc_q2_gemv(const uint16_t* x, const uint8_t* packed, int64_t m, int64_t n,
     }
 }
 
+/* Dense BF16 GEMM of the fallback prefill route (init_q2.rs, `qkvz_q2_prefill_gemm`:
+ * `dense_gemm_bf16_pipelined` after `dequant_q2_0_gn_to_bf16`): out[i][j] = sum over c of
+ * a[i][c] * w[j][c], the BF16 operands taken exactly, summed in fp64 in column order. */
+void orc_gemm_bf16(const uint16_t* a, const uint16_t* w, int64_t m, int64_t n, int64_t k, double* out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < m; i++)
+        for (int64_t j = 0; j < n; j++) {
+            double acc = 0.0;
+            for (int64_t c = 0; c < k; c++)
+                acc += (double)orc_bf16_to_f32(a[i * k + c]) * (double)orc_bf16_to_f32(w[j * k + c]);
+            out[i * n + j] = acc;
+        }
+}
+
 /* dense_ffn_decode_batch.rs, `forward_km_q2`: SiLU(gate) * up, rounded once to BF16.
  * SiLU(z) = z * sigmoid(z) = z / (1 + e^-z). */
 void orc_silu_mul_bf16(const uint16_t* gate, const uint16_t* up, int64_t count, uint16_t* out) {

@@ -396,6 +396,33 @@ def test_dequant_gemm_prefill_full(B, m):
     check_bf16_vs_f64(y[rows], ref, "dequant + gemm m=%d" % m)
 
 
+# ------------------------------------------------------------------------------ dense BF16 GEMM
+@pytest.mark.parametrize("m,n,k", [(1, 8, 64), (37, 300, 128), (128, 256, 64), (129, 257, 192), (300, 520, 1024),
+                                   (256, 512, 5120)])
+def test_dense_gemm_bf16_small(B, m, n, k):
+    """Every output element against the oracle: ragged m and n tails, one and several K
+    steps, several m and n tiles."""
+    g = synth._gen(1300 + m + n + k)
+    a = synth.activations(g, m, k)
+    w = synth.dense_weight(g, n, k)
+    y = bf16_dev_to_u16(B.dense_gemm_bf16(to_dev_u16_as_bf16(a), to_dev_u16_as_bf16(w)))
+    check_bf16_vs_f64(y, O.gemm_bf16(a, w), "dense gemm m=%d n=%d k=%d" % (m, n, k))
+
+
+def test_dense_gemm_bf16_edges(B):
+    import torch
+    a = torch.zeros((4, 64), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((8, 64), dtype=torch.bfloat16, device="cuda")
+    # k not a multiple of 64 is refused before any launch
+    with pytest.raises(B.BQ8Error):
+        B.dense_gemm_bf16(a[:, :48].contiguous(), w[:, :48].contiguous())
+    # k = 0 writes zeros
+    out = torch.full((4, 8), 3.0, dtype=torch.bfloat16, device="cuda")
+    B.dense_gemm_bf16(a[:, :0].contiguous(), w[:, :0].contiguous(), out=out)
+    assert torch.count_nonzero(out).item() == 0
+    assert B.lib().bq_device_status() == 0
+
+
 # ------------------------------------------------------------------------------ Q4_K MMQ
 @pytest.mark.parametrize("m,n,k", [(1, 8, 256), (5, 37, 512), (130, 300, 1024), (257, 129, 768), (64, 1000, 2048)])
 def test_q4k_mmq_small(B, m, n, k):

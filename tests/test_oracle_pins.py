@@ -175,6 +175,32 @@ def test_q2_gemv_closed_forms():
     assert np.array_equal(y2, -y)
 
 
+# --------------------------------------------------------------------------- dense BF16 GEMM
+def test_gemm_bf16_hand_product():
+    # a = [[1, 2, 3], [-1, 0.5, 4]], w = [[1, 0, -1], [2, 2, 2]] (all exact in BF16):
+    # out = a @ w^T = [[1 - 3, 2 + 4 + 6], [-1 - 4, -2 + 1 + 8]] = [[-2, 12], [-5, 7]]
+    a = bf16([[1, 2, 3], [-1, 0.5, 4]])
+    w = bf16([[1, 0, -1], [2, 2, 2]])
+    assert np.array_equal(O.gemm_bf16(a, w), np.array([[-2.0, 12.0], [-5.0, 7.0]]))
+
+
+def test_gemm_bf16_identity_and_shape():
+    g = np.random.default_rng(31)
+    m, k = 5, 64
+    a = bf16(g.standard_normal((m, k)))
+    eye = bf16(np.eye(k))
+    # w = I returns a exactly
+    assert np.array_equal(O.gemm_bf16(a, eye), O.bf16_to_f32(a).astype(np.float64))
+    # a non-square product against numpy's matmul of the same values: a transposed operand
+    # or a swapped index would change the shape or the values
+    n = 7
+    w = bf16(g.standard_normal((n, k)))
+    ref = O.bf16_to_f32(a).astype(np.float64) @ O.bf16_to_f32(w).astype(np.float64).T
+    out = O.gemm_bf16(a, w)
+    assert out.shape == (m, n)
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
 # --------------------------------------------------------------------------- SiLU*mul and FFN
 def test_silu_mul_matches_torch():
     rng = np.random.default_rng(3)
