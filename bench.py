@@ -99,7 +99,7 @@ class ClockSampler:
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_id, period_ms=20):
+    def __init__(self, gpu_id, period_ms=10):
         self.rows = []
         self.proc = None
         try:
@@ -270,6 +270,28 @@ def run_ours(args, rank, local, world):
     alg_bytes = wbytes + (K_HIDDEN * 2 + N_QKVZ * 2) * (1 + 4) / 2.0  # + x and y, averaged over m=1 and m=4
     achieved = alg_bytes / per_launch / 1e9
 
+    # the public API called eagerly (no CUDA graph): host marshalling, the tensor-map cache
+    # lookup and the launch, per call, against the same calls replayed from a graph
+    eager = {}
+    for m in (1, 4):
+        xm, ym = (x1, y1) if m == 1 else (x4, y4)
+        call = (lambda i: B.q2_gemv(xm, layers[i % L], out=ym[i % L])) if m == 1 else \
+            (lambda i: B.q2_gemv_batchm(xm, layers[i % L], out=ym[i % L]))
+        for i in range(3):
+            call(i)
+        torch.cuda.synchronize()
+        ncall = 400
+        h0 = time.perf_counter()
+        for i in range(ncall):
+            call(i)
+        h1 = time.perf_counter()
+        torch.cuda.synchronize()
+        h2 = time.perf_counter()
+        eager["m%d" % m] = {"host_us_per_call": round((h1 - h0) / ncall * 1e6, 2),
+                            "wall_us_per_call": round((h2 - h0) / ncall * 1e6, 2)}
+    eager["note"] = ("eager calls through the Python binding and the C ABI (tensor maps from the library's "
+                     "cache); host_us = time to issue a call, wall_us = issue to drain, per call")
+
     # per-m launch times: a graph of the L launches at one m, so host launch overhead is out
     kern = {}
     for m in (1, 4):
@@ -328,6 +350,7 @@ def run_ours(args, rank, local, world):
                      "kernel": "q2_gemv_hm_kernel", "peak_source": peak_src,
                      "note": "algorithmic bytes per launch (weight + x + y) / (graph elapsed / launches)"},
         "per_m": kern,
+        "eager": eager,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
@@ -588,7 +611,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--layers", type=int, default=16, help="distinct qkvz layer weights per step")
+    ap.add_argument("--layers", type=int, default=64,
+                    help="distinct qkvz layer weights per step (64: a step of about 1.7 ms, so that the clock "
+                         "sampler sees the timed region even at 20 steps)")
     ap.add_argument("--no-rows", action="store_true", help="headline only")
     ap.add_argument("--rows", default="gemv1024,ffn,prefill,q4k,nvfp4",
                     help="row groups to measure: gemv1024 (a1), ffn (a2-a4), prefill (a5, a6, a8, a9), q4k (a7), "
