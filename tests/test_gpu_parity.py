@@ -88,6 +88,28 @@ def test_q8_1_edge_values(B):
     assert np.array_equal(out, O.quantize_q8_1(bits))
 
 
+def test_q8_1_half_integer_boundaries(B):
+    """Blocks whose values sit on, and one or two BF16 steps beside, the points where
+    x / d is a half-integer (d = amax / 127): there the rounding of RN(x / d) decides the code,
+    so the kernel's reciprocal path must hand these values to the exact division."""
+    import torch
+    rng = np.random.default_rng(77)
+    m, k = 1024, 256
+    amax = (rng.uniform(0.5, 2.0, m) * np.exp2(rng.integers(-60, 60, m))).astype(np.float32)
+    amax_b = torch.tensor(amax).to(torch.bfloat16).to(torch.float32).numpy()
+    x = np.zeros((m, k), np.float32)
+    h = rng.integers(0, 127, size=(m, k)) + 0.5
+    x[:] = (h * amax_b[:, None] / 127.0) * rng.choice([-1.0, 1.0], size=(m, k))
+    xb = torch.tensor(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+    # one and two BF16 steps beside the half-integer points, in either direction
+    step = rng.integers(-2, 3, size=(m, k)).astype(np.int32)
+    xb = np.where(xb & 0x7FFF, (xb.astype(np.int32) + step) & 0xFFFF, xb).astype(np.uint16)
+    amax_bits = torch.tensor(amax_b).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    xb[:, ::32] = amax_bits[:, None]  # every 32-value block holds its row's amax
+    out = u8_dev(B.quantize_act_q8_1(to_dev_u16_as_bf16(xb)))
+    assert np.array_equal(out, O.quantize_q8_1(xb))
+
+
 # ------------------------------------------------------------------------------ NVFP4 -> BF16
 def _nvfp4(B, d, scale2=None):
     import torch
