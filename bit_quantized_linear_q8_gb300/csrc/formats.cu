@@ -136,7 +136,8 @@ __global__ void __launch_bounds__(256) q8_1_kernel(const uint16_t* __restrict__ 
 // =====================================================================================
 // NVFP4 -> BF16: w = e2m1(code) * e4m3(scale) * scale2, the exact product rounded once to
 // BF16.  Layout: codes [n][k/2] bytes (value 2j in the low nibble of byte j), one E4M3
-// scale byte per 16 values [n][k/16].  One CTA per row, 256 threads (the page's launch).
+// scale byte per 16 values [n][k/16].  (The page launches one CTA of 256 threads per row;
+// here one thread takes one 16-value group of the flattened weight, see below.)
 // e2m1 * e4m3 is exact in fp32; the product with scale2 is taken with round-to-odd in
 // fp32 (truncate, then set the last bit if the FMA residual is nonzero), and rounding
 // that to BF16 to nearest equals rounding the exact product once, because fp32 carries
@@ -174,37 +175,73 @@ __device__ __forceinline__ uint32_t nv_bf16_exact(float a, float s2) {
     return *reinterpret_cast<const uint16_t*>(&h);
 }
 
+// One 32-bit word of codes (8 values) through the group's table: lo / hi hold the low and
+// high bytes of T[0..7], T[i] the BF16 of e2m1 magnitude i (0, .5, 1, 1.5, 2, 3, 4, 6) times
+// sc * scale2; each nibble's low three bits index T by byte permutes, its bit 3 flips the
+// sign.  o[0..3] receive values (0, 1) .. (6, 7) of the word.
+__device__ __forceinline__ void nv_word_lookup(uint32_t w, uint32_t lo0, uint32_t lo1, uint32_t hi0, uint32_t hi1,
+                                               uint32_t* o) {
+    const uint32_t v = w << 4;  // byte k of v carries the sign of byte k's low nibble in bit 7
+#pragma unroll
+    for (int p = 0; p < 2; p++) {
+        const uint32_t sel = (w >> (16 * p)) & 0x7777u;  // magnitude indices of four values
+        const uint32_t a = __byte_perm(lo0, lo1, sel), b = __byte_perm(hi0, hi1, sel);
+        const uint32_t s0 = __byte_perm(w, v, p ? 0x2060u : 0x0040u);  // signs of values 4p, 4p + 1
+        const uint32_t s1 = __byte_perm(w, v, p ? 0x3070u : 0x1050u);  // and 4p + 2, 4p + 3
+        o[2 * p] = __byte_perm(a, b, 0x5140u) ^ (s0 & 0x80008000u);
+        o[2 * p + 1] = __byte_perm(a, b, 0x7362u) ^ (s1 & 0x80008000u);
+    }
+}
+
+// The [n][k] weight is a flat sequence of n k / 16 groups of 16 values (8 code bytes, one
+// scale byte, 32 output bytes), contiguous across rows; a full-occupancy grid strides over
+// them, so a warp reads 256 contiguous code bytes and writes 1 KB per step.
+// Per group the sixteen products are power-of-two multiples of Q = sc * scale2 or of 1.5 Q,
+// so two exactly rounded values b1 = BF16(Q) and b3 = BF16(1.5 Q) give all eight magnitudes
+// by exponent adds (exact while the results stay normal BF16 numbers); groups where they
+// would not (zero, huge or tiny Q, a NaN scale) take the per-value path.
 __global__ void __launch_bounds__(256) nvfp4_dequant_kernel(const uint8_t* __restrict__ packed,
                                                             const uint8_t* __restrict__ scales,
-                                                            uint16_t* __restrict__ out, float scale2, int k) {
-    const int64_t r = blockIdx.x;
-    const uint8_t* prow = packed + r * (k / 2);
-    const uint8_t* srow = scales + r * (k / 16);
-    uint16_t* orow = out + r * k;
-    for (int g = threadIdx.x; g < k / 16; g += blockDim.x) {  // 16 values: 8 code bytes, 1 scale
-        const uint2 c = *reinterpret_cast<const uint2*>(prow + 8 * g);
-        const float sc = nv_e4m3(srow[g]);
-        float a[16];
-        uint32_t o[8], tiny = 0;
+                                                            uint16_t* __restrict__ out, float scale2,
+                                                            int64_t ngroups) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < ngroups; g += stride) {
+        const uint2 c = __ldg(reinterpret_cast<const uint2*>(packed + 8 * g));
+        const float sc = nv_e4m3(__ldg(scales + g));
+        uint32_t o[8];
+        uint32_t t1, t3;
+        const uint32_t b1 = nv_bf16_fast(sc, scale2, t1);
+        const uint32_t b3 = nv_bf16_fast(1.5f * sc, scale2, t3);  // 1.5 sc is exact
+        const uint32_t e1 = (b1 >> 7) & 0xFFu, e3 = (b3 >> 7) & 0xFFu;
+        if ((t1 | t3) == 0u && e1 >= 2u && e1 <= 252u && e3 >= 1u && e3 <= 252u) {
+            // T = (+-0, Q/2, Q, 1.5Q, 2Q, 3Q, 4Q, 6Q) as BF16, the zero with Q's sign
+            const uint32_t p01 = (b1 & 0x8000u) | ((b1 - 128u) << 16), p23 = b1 | (b3 << 16);
+            const uint32_t p45 = (b1 + 128u) | ((b3 + 128u) << 16), p67 = (b1 + 256u) | ((b3 + 256u) << 16);
+            const uint32_t lo0 = __byte_perm(p01, p23, 0x6420u), hi0 = __byte_perm(p01, p23, 0x7531u);
+            const uint32_t lo1 = __byte_perm(p45, p67, 0x6420u), hi1 = __byte_perm(p45, p67, 0x7531u);
+            nv_word_lookup(c.x, lo0, lo1, hi0, hi1, o);
+            nv_word_lookup(c.y, lo0, lo1, hi0, hi1, o + 4);
+        } else {
+            float a[16];
+            uint32_t tiny = 0;
 #pragma unroll
-        for (int j = 0; j < 8; j++) {
-            const uint32_t byte = ((j < 4 ? c.x : c.y) >> (8 * (j & 3))) & 0xFFu;
-            a[2 * j] = nv_e2m1(byte & 15u) * sc;  // exact
-            a[2 * j + 1] = nv_e2m1(byte >> 4) * sc;
-            uint32_t t0, t1;
-            o[j] = nv_bf16_fast(a[2 * j], scale2, t0) | (nv_bf16_fast(a[2 * j + 1], scale2, t1) << 16);
-            tiny |= (t0 << (2 * j)) | (t1 << (2 * j + 1));
-        }
-        if (__any_sync(__activemask(), tiny != 0u)) {  // rare: redo the tiny products exactly
+            for (int j = 0; j < 8; j++) {
+                const uint32_t byte = ((j < 4 ? c.x : c.y) >> (8 * (j & 3))) & 0xFFu;
+                a[2 * j] = nv_e2m1(byte & 15u) * sc;  // exact
+                a[2 * j + 1] = nv_e2m1(byte >> 4) * sc;
+                uint32_t u0, u1;
+                o[j] = nv_bf16_fast(a[2 * j], scale2, u0) | (nv_bf16_fast(a[2 * j + 1], scale2, u1) << 16);
+                tiny |= (u0 << (2 * j)) | (u1 << (2 * j + 1));
+            }
 #pragma unroll
-            for (int e = 0; e < 16; e++) {
+            for (int e = 0; e < 16; e++) {  // products near the BF16 subnormal range, exactly
                 if ((tiny >> e) & 1u) {
                     const uint32_t v = nv_bf16_exact(a[e], scale2);
                     o[e >> 1] = (e & 1) ? ((o[e >> 1] & 0xFFFFu) | (v << 16)) : ((o[e >> 1] & 0xFFFF0000u) | v);
                 }
             }
         }
-        uint4* dst = reinterpret_cast<uint4*>(orow + 16 * g);
+        uint4* dst = reinterpret_cast<uint4*>(out + 16 * g);
         dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
         dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
     }
@@ -378,8 +415,9 @@ int dequant_nvfp4_to_bf16(const void* packed, const void* scales, uint16_t* out,
     if (!aligned16(packed) || !aligned16(out))
         return fail(BQ_ERR_INVALID, "%s: packed and out must be 16-byte aligned", who);
     if (n > 0x7FFFFFFFu || k > (1u << 30)) return fail(BQ_ERR_INVALID, "%s: shape too large", who);
-    nvfp4_dequant_kernel<<<n, 256, 0, (cudaStream_t)stream>>>((const uint8_t*)packed, (const uint8_t*)scales, out,
-                                                              scale2, (int)k);
+    const int64_t ngroups = (int64_t)n * (k / 16);
+    nvfp4_dequant_kernel<<<grid_for(ngroups, 256), 256, 0, (cudaStream_t)stream>>>(
+        (const uint8_t*)packed, (const uint8_t*)scales, out, scale2, ngroups);
     return check_launch(who);
 }
 

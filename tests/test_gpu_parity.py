@@ -137,6 +137,24 @@ def test_nvfp4_dequant_edges(B):
         assert np.array_equal(out, ref), s2
 
 
+def test_nvfp4_dequant_every_code_and_scale(B):
+    """Every (scale byte, code byte) pair, under scale2 values from the BF16 subnormal range
+    to overflow: the kernel's per-group table (exponent adds of BF16(Q) and BF16(1.5 Q)) and
+    its per-value fallback must both give the oracle's bits."""
+    n, k = 256, 512  # row r: scale byte r for all 32 groups; every code byte once per row
+    packed = np.tile(np.arange(256, dtype=np.uint8), (n, 1))
+    scales = np.repeat(np.arange(256, dtype=np.uint8)[:, None], k // 16, axis=1)
+    d = dict(n=n, k=k, packed=packed, scales=scales, scale2=1.0)
+    nan_rows = np.array([0x7F, 0xFF])  # E4M3 NaN scales: NaN outputs, bit pattern unspecified
+    ok_rows = np.setdiff1d(np.arange(n), nan_rows)
+    for s2 in (0.0021, -0.37, 1.0, 2.0 ** -120, 3e-39, 2.0 ** 118, 1e36):
+        out, ref = _nvfp4(B, d, s2)
+        bad = np.argwhere(out[ok_rows] != ref[ok_rows])
+        assert bad.size == 0, "scale2 %g: %d differ, first (scale byte, value) %s: got %04x want %04x" % (
+            s2, len(bad), (ok_rows[bad[0][0]], bad[0][1]), out[ok_rows][tuple(bad[0])], ref[ok_rows][tuple(bad[0])])
+        assert np.all((out[nan_rows] & 0x7FFF) > 0x7F80)
+
+
 def test_nvfp4_dequant_full(B):
     out, ref = _nvfp4(B, synth.nvfp4_ffn_weight())
     assert np.array_equal(out, ref)
