@@ -233,7 +233,7 @@ __device__ __forceinline__ void qt_epilogue(uint32_t tA, int c0, int c1, int row
 __global__ void __launch_bounds__(512, 1)
     q2_mmq_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapD,
                      const __grid_constant__ CUtensorMap mapB, const uint16_t* __restrict__ wsc,
-                     uint16_t* __restrict__ out, int m, int n, int k, int ntn) {
+                     uint16_t* __restrict__ out, int m, int n, int k, int ntm) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* bst = align1024(smem_raw);
     uint8_t* ring = bst + QT_NS * QT_BSTAGE;
@@ -247,7 +247,9 @@ __global__ void __launch_bounds__(512, 1)
     volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int n0 = (blockIdx.x % ntn) * QT_BN, m0 = (blockIdx.x / ntn) * QT_BM;
+    // m tiles vary fastest: the CTAs resident at once share few weight tiles, each weight tile
+    // is read from HBM once while the activations stay in L2
+    const int m0 = (blockIdx.x % ntm) * QT_BM, n0 = (blockIdx.x / ntm) * QT_BN;
     const int S = k >> 6;  // K steps of 64
     const int G = k >> 7;  // groups of 128 (one BF16 scale each)
 
@@ -510,7 +512,7 @@ __device__ __forceinline__ void q4t_split_pair(uint32_t nib, uint32_t sel0, uint
 __global__ void __launch_bounds__(512, 1)
     q4k_mmq_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapD,
                       const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapH,
-                      uint16_t* __restrict__ out, int m, int n, int k, int ntn) {
+                      uint16_t* __restrict__ out, int m, int n, int k, int ntm) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* bst = align1024(smem_raw);
     uint8_t* ring = bst + Q4T_NSB * Q4T_BSTAGE;
@@ -525,7 +527,9 @@ __global__ void __launch_bounds__(512, 1)
     volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int n0 = (blockIdx.x % ntn) * QT_BN, m0 = (blockIdx.x / ntn) * QT_BM;
+    // m tiles vary fastest: the CTAs resident at once share few weight tiles, each weight tile
+    // is read from HBM once while the activations stay in L2
+    const int m0 = (blockIdx.x % ntm) * QT_BM, n0 = (blockIdx.x / ntm) * QT_BN;
     const int S = k >> 6;
 
     if (threadIdx.x == 0) {
@@ -744,11 +748,11 @@ extern "C" int q2_mmq_gemm(const void* act_q8, const bq_q2_weight* w, uint16_t* 
     if ((st = make_tmap_2d_u8(&mB, wcodes, k / 4, n, k / 4, 16, QT_BN, false, who))) return st;
     static int cache[64] = {0};
     if ((st = qt_reserve_smem((const void*)q2_mmq_tc_kernel, cache, QT_SMEM, who))) return st;
-    const int ntn = (int)((n + QT_BN - 1) / QT_BN);
-    const uint64_t tiles = (uint64_t)ntn * ((m + QT_BM - 1) / QT_BM);
+    const int ntm = (int)((m + QT_BM - 1) / QT_BM);
+    const uint64_t tiles = (uint64_t)ntm * ((n + QT_BN - 1) / QT_BN);
     if (tiles > 0x7FFFFFFFull) return fail(BQ_ERR_INVALID, "%s: shape too large", who);
     q2_mmq_tc_kernel<<<(unsigned)tiles, QT_THREADS, QT_SMEM, (cudaStream_t)stream>>>(mA, mD, mB, wsc, out, (int)m,
-                                                                                   (int)n, (int)k, ntn);
+                                                                                   (int)n, (int)k, ntm);
     return check_launch(who);
 }
 
@@ -781,10 +785,10 @@ extern "C" int q4k_mmq_gemm(const void* act_q8, const void* w_q4k, uint16_t* out
     if ((st = make_tmap_3d_u8(&mH, w_q4k, {16, n, wrow / 16}, {wrow, 16}, {16, QT_BN, 1}, who))) return st;
     static int cache[64] = {0};
     if ((st = qt_reserve_smem((const void*)q4k_mmq_tc_kernel, cache, Q4T_SMEM, who))) return st;
-    const int ntn = (int)((n + QT_BN - 1) / QT_BN);
-    const uint64_t tiles = (uint64_t)ntn * ((m + QT_BM - 1) / QT_BM);
+    const int ntm = (int)((m + QT_BM - 1) / QT_BM);
+    const uint64_t tiles = (uint64_t)ntm * ((n + QT_BN - 1) / QT_BN);
     if (tiles > 0x7FFFFFFFull) return fail(BQ_ERR_INVALID, "%s: shape too large", who);
     q4k_mmq_tc_kernel<<<(unsigned)tiles, Q4T_THREADS, Q4T_SMEM, (cudaStream_t)stream>>>(mA, mD, mQ, mH, out, (int)m,
-                                                                                      (int)n, (int)k, ntn);
+                                                                                      (int)n, (int)k, ntm);
     return check_launch(who);
 }
