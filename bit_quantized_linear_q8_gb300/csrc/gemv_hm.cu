@@ -99,6 +99,24 @@ struct HmLayout {
     }
 };
 
+// Shared-memory loads by 32-bit shared address (volatile: never moved across the barrier
+// waits that publish the data).
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float lds_bf16(uint32_t a) {  // one BF16 value as fp32
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return __uint_as_float((uint32_t)v << 16);
+}
+
 // Waits on phase `parity` of `bar` (suspending, bounded); the answer is the warp's, so the
 // warp-synchronous MMAs that follow run with every lane or none.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
@@ -183,6 +201,44 @@ struct HmCursor {
         }
     }
 };
+
+// One block step of a warp: the 8 MMAs of pack block pb for the first NT tiles of its pair.
+// c: the lane's code bytes of row g of the first tile (row g + 8 is 1024 bytes on, the
+// second tile q1_off on); b: the lane's 64 bytes of B fragments (quads M * 64 bytes apart);
+// s: the scale of row g of the first tile (row g + 8 at g8, the second tile at q1_s).
+template <int NT, int M>
+__device__ __forceinline__ void hm_block(float (&tot)[HM_TG][4], uint32_t c, uint32_t q1_off, uint32_t b, uint32_t s,
+                                         uint32_t q1_s, uint32_t g8) {
+    uint2 w[HM_TG], w8[HM_TG];
+    w[0] = lds64(c);
+    w8[0] = lds64(c + 8 * 128);
+    w[1] = w8[1] = make_uint2(0u, 0u);
+    if (NT == 2) {
+        w[1] = lds64(c + q1_off);
+        w8[1] = lds64(c + q1_off + 8 * 128);
+    }
+    uint32_t bf[16];
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+        const uint4 v = lds128(b + (uint32_t)e * (64u * M));
+        bf[4 * e] = v.x;
+        bf[4 * e + 1] = v.y;
+        bf[4 * e + 2] = v.z;
+        bf[4 * e + 3] = v.w;
+    }
+    float ac[HM_TG][4];
+#pragma unroll
+    for (int q = 0; q < HM_TG; q++) ac[q][0] = ac[q][1] = ac[q][2] = ac[q][3] = 0.f;
+    hm_tiles<NT>(ac, w, w8, bf);
+#pragma unroll
+    for (int q = 0; q < NT; q++) {
+        const float d0 = lds_bf16(s + q * q1_s), d8 = lds_bf16(s + q * q1_s + g8);
+        tot[q][0] = fmaf(d0, ac[q][0], tot[q][0]);
+        tot[q][1] = fmaf(d0, ac[q][1], tot[q][1]);
+        tot[q][2] = fmaf(d8, ac[q][2], tot[q][2]);
+        tot[q][3] = fmaf(d8, ac[q][3], tot[q][3]);
+    }
+}
 
 __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"r"(HM_CWARPS * 32) : "memory");
@@ -410,6 +466,14 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
     const size_t pstride = (size_t)16 * p.tmax * M;  // one part's (and weight's) partial sums
     // second tile of a pair: the next tile of the box, or the same tile of the up weight
     const uint32_t q1_off = DUAL ? 2 * box_bytes : HM_BOX;
+    const uint32_t ring32 = smem_u32(ring), srow32 = smem_u32(srow);
+    const uint32_t lane_c = (uint32_t)(g * 128 + ((t & 1) << 3));               // row g, 8-byte half of a chunk
+    const uint32_t bbase = smem_u32(btab) + (uint32_t)(jb * 4 + t) * 16u;       // + pb * 256 m
+    const uint32_t q1_s2 = DUAL ? (uint32_t)L.scal_w : 32u * (uint32_t)G;       // second tile's scales
+    const uint32_t G8 = 16u * (uint32_t)G;                                       // 8 rows of scales
+    // the 128-byte swizzle maps 16-byte chunk j of box row r to chunk j ^ (r & 7); rows g and
+    // g + 8 share r & 7 = g
+    auto swz = [&](int blk) { return (uint32_t)(((((blk & 3) << 1) | (t >> 1)) ^ g) << 4); };
     float tot[HM_TG][4];
 #pragma unroll
     for (int q = 0; q < HM_TG; q++) tot[q][0] = tot[q][1] = tot[q][2] = tot[q][3] = 0.f;
@@ -420,51 +484,28 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
         // tiles of this warp's pair (<= 0: none) and its first tile in the CTA
         const int ntp = DUAL ? (pair < ntg ? 2 : 0) : min(HM_TG, ntg - HM_TG * pair);
         const int tile0 = ch.gi * TGB + (DUAL ? pair : HM_TG * pair);
-        if (ntp > 0 && part < 8) {
-            const uint8_t* sbase = ring + (size_t)ch.s * stage_bytes + (size_t)(tile0 - ch.gi * TGB) * HM_BOX +
-                                   g * 128 + ((t & 1) << 3);
-            for (int bi = 0; bi < nbw; bi++) {
-                const int blk = part + bi * wpp;  // pack block within the chunk, 0..7
-                const int pb = ch.kc * 8 + blk;
-                if (pb >= P) break;
-                // the 128-byte swizzle maps 16-byte chunk j of box row r to chunk j ^ (r & 7);
-                // rows g and g + 8 share r & 7 = g
-                const uint8_t* cb = sbase + (size_t)(blk >> 2) * box_bytes + (((((blk & 3) << 1) | (t >> 1)) ^ g) << 4);
-                uint2 w[HM_TG], w8[HM_TG];
-                w[0] = *reinterpret_cast<const uint2*>(cb);
-                w8[0] = *reinterpret_cast<const uint2*>(cb + 8 * 128);
-                w[1] = w8[1] = make_uint2(0u, 0u);
-                if (ntp == 2) {
-                    w[1] = *reinterpret_cast<const uint2*>(cb + q1_off);
-                    w8[1] = *reinterpret_cast<const uint2*>(cb + q1_off + 8 * 128);
+        if (ntp > 0) {
+            // 32-bit shared addresses: this warp's code bytes of the pair's first tile in the
+            // stage (row g; the block's swizzled 16-byte chunk is added per block), its B
+            // fragments (block pb at pb * 256 m bytes) and its scales (block pb at (pb >> gsh) * 2)
+            const uint32_t cbase = ring32 + (uint32_t)ch.s * stage_bytes + (uint32_t)(tile0 - ch.gi * TGB) * HM_BOX + lane_c;
+            const uint32_t sbase = srow32 + (uint32_t)(tile0 * 16 + g) * (uint32_t)G * 2u;
+            const int pb0 = ch.kc * 8;
+            if (ntp == 2) {
+                for (int bi = 0; bi < nbw; bi++) {
+                    const int blk = part + bi * wpp;  // pack block within the chunk, 0..7
+                    const int pb = pb0 + blk;
+                    if (pb >= P) break;
+                    hm_block<2, M>(tot, cbase + (uint32_t)(blk >> 2) * box_bytes + swz(blk), q1_off,
+                                   bbase + (uint32_t)pb * (256u * M), sbase + (uint32_t)(pb >> gsh) * 2u, q1_s2, G8);
                 }
-                uint32_t b[16];
-                const uint4* bp = reinterpret_cast<const uint4*>(btab + (((size_t)pb * 4 * M + jb) * 4 + t) * 16);
-#pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    const uint4 v = bp[(size_t)e * M * 4];
-                    b[4 * e] = v.x;
-                    b[4 * e + 1] = v.y;
-                    b[4 * e + 2] = v.z;
-                    b[4 * e + 3] = v.w;
-                }
-                float ac[HM_TG][4];
-#pragma unroll
-                for (int q = 0; q < HM_TG; q++) ac[q][0] = ac[q][1] = ac[q][2] = ac[q][3] = 0.f;
-                if (ntp == 2) hm_tiles<2>(ac, w, w8, b);
-                else hm_tiles<1>(ac, w, w8, b);
-                const uint16_t* sg = srow + (size_t)(tile0 * 16 + g) * G + (pb >> gsh);
-                // the second tile's scales: 16 rows on, or the up weight's rows
-                const size_t q1_s = DUAL ? L.scal_w / 2 : (size_t)16 * G;
-#pragma unroll
-                for (int q = 0; q < HM_TG; q++) {
-                    if (q >= ntp) continue;  // a one-tile pair: the second tile's scales do not exist
-                    const float d0 = bf16_bits_to_f32(sg[q * q1_s]);
-                    const float d8 = bf16_bits_to_f32(sg[q * q1_s + (size_t)8 * G]);
-                    tot[q][0] = fmaf(d0, ac[q][0], tot[q][0]);
-                    tot[q][1] = fmaf(d0, ac[q][1], tot[q][1]);
-                    tot[q][2] = fmaf(d8, ac[q][2], tot[q][2]);
-                    tot[q][3] = fmaf(d8, ac[q][3], tot[q][3]);
+            } else {
+                for (int bi = 0; bi < nbw; bi++) {
+                    const int blk = part + bi * wpp;
+                    const int pb = pb0 + blk;
+                    if (pb >= P) break;
+                    hm_block<1, M>(tot, cbase + (uint32_t)(blk >> 2) * box_bytes + swz(blk), q1_off,
+                                   bbase + (uint32_t)pb * (256u * M), sbase + (uint32_t)(pb >> gsh) * 2u, q1_s2, G8);
                 }
             }
         }
