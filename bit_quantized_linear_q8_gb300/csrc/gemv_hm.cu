@@ -30,7 +30,9 @@
 //    of 2 KB stream at a fifth of the rate of 16 KB ones.  A producer warp requests the
 //    chunks into a ring (mbarrier "full" per stage, transaction bytes) and refills a stage
 //    once every consumer warp has arrived on its "empty" barrier; the ring usually holds the
-//    CTA's whole slice, so it is all requested at once, with the CTA's scales (one bulk copy).
+//    CTA's whole slice.  The first chunk and the CTA's scales (one bulk copy) are requested at
+//    once, the rest as soon as the activations have arrived (a deeper early prefetch queues
+//    the activation loads, which every warp waits for, behind weight bytes).
 //    The tensor maps come from a process-wide cache.  Every wait is bounded.
 //  * Compute: sixteen consumer warps.  Warp w takes the tile pair w / P' of every row group
 //    (two independent MMA chains) and pack blocks w % P', w % P' + P', ... of every chunk
@@ -50,6 +52,10 @@ constexpr int HM_TG = 2;                          // tiles per MMA step (two cha
 constexpr int HM_MAX_TGB = 8;                     // tiles per row group (one box height)
 constexpr int HM_BOX = 16 * 128;                  // one box: 16 rows x 128 bytes
 constexpr int HM_SMEM_LIMIT = 225 * 1024;
+// Chunks requested before the activations have arrived: the SM's memory queue serves requests
+// roughly in order, so a deep weight prefetch would hold back the activation loads that every
+// warp waits for, while the weight stream has time to spare behind the table build.
+constexpr int HM_EARLY_CHUNKS = 1;
 
 static __device__ unsigned int g_hm_status;
 
@@ -95,7 +101,7 @@ struct HmLayout {
         scal_w = ((size_t)tmax * 16 * G * 2 + 32 + 15) & ~size_t(15);
         slot = scal + nw * scal_w;                                      // [parts][nw][16 tmax rows][m] fp32
         misc = slot + (size_t)hm_parts(tgb, nw) * nw * 16 * tmax * m * 4;  // barriers, row maxima, row scales
-        total = misc + 2 * HM_MAX_STAGES * 8 + 8 + 8 * 4 * 2 + 1024;    // + alignment
+        total = misc + 2 * HM_MAX_STAGES * 8 + 16 + 8 * 4 * 2 + 1024;   // + alignment
     }
 };
 
@@ -262,7 +268,8 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.misc);
     uint64_t* empty = full + HM_MAX_STAGES;
     uint64_t* sbar = empty + HM_MAX_STAGES;
-    uint32_t* rowmax = reinterpret_cast<uint32_t*>(sbar + 1);
+    uint64_t* xready = sbar + 1;  // the activations have arrived (the first table pass is done)
+    uint32_t* rowmax = reinterpret_cast<uint32_t*>(xready + 1);
     float* rowback = reinterpret_cast<float*>(rowmax + 8);  // 2^-s per activation row
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -296,6 +303,7 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
             mbar_init(&empty[s], HM_CWARPS);
         }
         mbar_init(sbar, 1);
+        mbar_init(xready, 1);
         fence_barrier_init();
     }
     if (tid < 8) rowmax[tid] = 0u;
@@ -322,7 +330,12 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
             int nis = 0;  // chunks requested
             HmCursor cur = {0, 0, 0, 0u};
             for (int c = 0; c < nch; c++) {
-                // stage cur.s is free once the eight consumers released its previous chunk
+                // the rest of the weight waits until the activations have arrived
+                if (c == HM_EARLY_CHUNKS && !mbar_wait_suspend(xready, 0)) {
+                    ok = false;
+                    break;
+                }
+                // stage cur.s is free once every consumer released its previous chunk
                 if (c >= NST && !mbar_wait_suspend(&empty[cur.s], cur.ph ^ 1u)) {
                     ok = false;
                     break;
@@ -336,7 +349,7 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
                         tma_load_2d(dst + (size_t)(w * 2 + h) * box_bytes, w ? &tmap2 : &tmap, cur.kc * 256 + h * 128,
                                     r0 + 16 * cur.gi * TGB, &full[cur.s]);
                 nis++;
-                if (c == NST - 1 && nch > NST) {
+                if (c == (NST - 1 > HM_EARLY_CHUNKS ? NST - 1 : HM_EARLY_CHUNKS) && nch > NST) {
                     // the ring is full: the CTA's later row groups into L2, 64 KB per request
                     const size_t total = (size_t)R * kb;
                     for (int w = 0; w < NW; w++) {
@@ -404,6 +417,7 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
         }
     }
     consumer_sync();
+    if (tid == 0) mbar_arrive(xready);
     if (tid < M) {
         const uint32_t mb = rowmax[tid];
         int sh = mb ? 14 - (int)((mb >> 23) & 0xFF) + 127 : 0;
