@@ -10,12 +10,17 @@
 //    stages of 16 KB (a) + 32 KB (w) in shared memory; the MMAs read them through
 //    shared-memory descriptors (swizzle 128B, 8-row groups 1024 bytes apart, each K16 slice
 //    32 bytes further into the swizzle atom).
-//  * The accumulator (128 lanes x 256 fp32 columns) lives in tensor memory.
-//  * Warp 1 (one lane) streams the tiles; warp 0 allocates tensor memory and one lane issues
+//  * Persistent grid: one CTA per SM (at most one per tile) walks the tiles id = blockIdx.x,
+//    + gridDim.x, ..., m tiles varying fastest.
+//  * Two accumulators (128 lanes x 256 fp32 columns each, all 512 tensor-memory columns):
+//    tile i of a CTA accumulates into buffer i % 2, so the epilogue of one tile overlaps the
+//    MMAs of the next.
+//  * Warp 1 (one lane) streams the K steps of all the CTA's tiles through the stage ring
+//    without a break at tile boundaries; warp 0 allocates tensor memory and one lane issues
 //    the M128 N256 K16 MMAs (four per K step), committing each step to the stage's `empty`
-//    barrier and the last one to `done`; warps 4-7 (one tensor-memory lane quadrant each,
-//    one output row per thread) read the accumulator with tcgen05.ld and store BF16.
-//  * Grid: one CTA per output tile, m tiles varying fastest.
+//    barrier and each tile's last step to the buffer's `full` barrier; warps 4-7 (one
+//    tensor-memory lane quadrant each, one output row per thread) read a finished buffer
+//    with tcgen05.ld, store BF16 and hand the buffer back through its `empty` barrier.
 //  * Every wait is bounded; a wait that gives up raises the CTA's abort flag and the status
 //    word, and the kernel winds down (the MMA warp still waits for its own MMAs before the
 //    tensor memory is freed).
@@ -41,9 +46,9 @@ constexpr uint32_t GB_ASTAGE = GB_BM * GB_BK * 2;      // 16 KB
 constexpr uint32_t GB_BSTAGE = GB_BN * GB_BK * 2;      // 32 KB
 constexpr uint32_t GB_STAGE = GB_ASTAGE + GB_BSTAGE;
 constexpr int GB_THREADS = 8 * 32;
-constexpr uint32_t GB_TMEM_COLS = 256;
+constexpr uint32_t GB_TMEM_COLS = 512;                 // two 256-column accumulators
 constexpr uint32_t GB_WAIT_LIMIT = 1u << 20;           // try_waits before a wait gives up
-constexpr size_t GB_SMEM = 1024 + (size_t)GB_NS * GB_STAGE + (2 * GB_NS + 1) * 8 + 16;
+constexpr size_t GB_SMEM = 1024 + (size_t)GB_NS * GB_STAGE + (2 * GB_NS + 5) * 8 + 16;
 static_assert(GB_SMEM <= 227 * 1024, "shared memory budget");
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bit 4), A and B BF16 (bits 7-9,
@@ -109,25 +114,33 @@ __device__ __forceinline__ void gb_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 // (Launch bounds of 256 threads: eight warps, two per SM sub-partition.)
 __global__ void __launch_bounds__(GB_THREADS, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapW,
-                        uint16_t* __restrict__ out, int m, int n, int k, int ntm) {
+                        uint16_t* __restrict__ out, int m, int n, int k, int ntm, int ntiles) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* stages = align1024(smem_raw);  // [stage][a 128 x 64 | w 256 x 64] BF16, 128-byte swizzle
     uint64_t* full = reinterpret_cast<uint64_t*>(stages + GB_NS * GB_STAGE);
     uint64_t* empty = full + GB_NS;
-    uint64_t* done = empty + GB_NS;
+    uint64_t* accf = empty + GB_NS;  // [2] accumulator buffer holds a finished tile
+    uint64_t* acce = accf + 2;       // [2] accumulator buffer read out by the epilogue
+    uint64_t* done = acce + 2;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 1);
     volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // m tiles vary fastest: the CTAs resident at once share few weight tiles, and the
-    // activations (m x k) stay in L2 while each weight tile is read once
-    const int m0 = (blockIdx.x % ntm) * GB_BM, n0 = (blockIdx.x / ntm) * GB_BN;
     const int S = k / GB_BK;
+    const int G = gridDim.x;
+    // tile id -> (m0, n0) with m tiles varying fastest: the tiles in flight at once (ids
+    // i G .. (i + 1) G - 1) share few weight tiles, and the activations stay in L2
+    auto tile_m0 = [&](int id) { return (id % ntm) * GB_BM; };
+    auto tile_n0 = [&](int id) { return (id / ntm) * GB_BN; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < GB_NS; s++) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&accf[b], 1);
+            mbar_init(&acce[b], 4);  // one arrival per epilogue warp
         }
         mbar_init(done, 1);
         *abort = 0;
@@ -145,35 +158,57 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
 
     if (warp == 1) {
         // ---------------------------------------------------------------- TMA producer
+        // one continuous stream of K steps over the CTA's tiles
         if (lane == 0) {
-            int issued = 0;
-            for (int s = 0; s < S; s++) {
-                const int st = s % GB_NS;
-                if (s >= GB_NS && !gb_wait(&empty[st], (uint32_t)((s / GB_NS) - 1) & 1u, abort)) break;
-                uint8_t* dst = stages + (size_t)st * GB_STAGE;
-                mbar_arrive_expect_tx(&full[st], GB_STAGE);
-                tma_load_2d(dst, &mapA, s * GB_BK * 2, m0, &full[st]);
-                tma_load_2d(dst + GB_ASTAGE, &mapW, s * GB_BK * 2, n0, &full[st]);
-                issued++;
+            int64_t it = 0;
+            bool ok = true;
+            for (int id = blockIdx.x; id < ntiles && ok; id += G) {
+                const int m0 = tile_m0(id), n0 = tile_n0(id);
+                for (int ks = 0; ks < S; ks++, it++) {
+                    const int st = (int)(it % GB_NS);
+                    if (it >= GB_NS && !gb_wait(&empty[st], (uint32_t)((it / GB_NS) - 1) & 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* dst = stages + (size_t)st * GB_STAGE;
+                    mbar_arrive_expect_tx(&full[st], GB_STAGE);
+                    tma_load_2d(dst, &mapA, ks * GB_BK * 2, m0, &full[st]);
+                    tma_load_2d(dst + GB_ASTAGE, &mapW, ks * GB_BK * 2, n0, &full[st]);
+                }
             }
             // wind down: every copy requested must have landed before the CTA exits
-            for (int s = issued > GB_NS ? issued - GB_NS : 0; s < issued; s++)
-                if (!mbar_wait_suspend(&full[s % GB_NS], (uint32_t)(s / GB_NS) & 1u)) atomicOr(&g_gemm_status, 2u);
+            for (int64_t j = it > GB_NS ? it - GB_NS : 0; j < it; j++)
+                if (!mbar_wait_suspend(&full[j % GB_NS], (uint32_t)(j / GB_NS) & 1u)) atomicOr(&g_gemm_status, 2u);
         }
         __syncwarp();
     } else if (warp == 0) {
         // ---------------------------------------------------------------- MMA issuer
+        // tile i of the CTA accumulates into buffer i % 2 (columns 256 (i % 2) ..) once the
+        // epilogue has read out tile i - 2
         if (lane == 0) {
-            for (int s = 0; s < S; s++) {
-                const int st = s % GB_NS;
-                if (!gb_wait(&full[st], (uint32_t)(s / GB_NS) & 1u, abort)) break;
+            int64_t it = 0;
+            bool ok = true;
+            int ti = 0;
+            for (int id = blockIdx.x; id < ntiles && ok; id += G, ti++) {
+                const int buf = ti & 1;
+                if (ti >= 2 && !gb_wait(&acce[buf], (uint32_t)((ti >> 1) - 1) & 1u, abort)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t abase = smem_u32(stages + (size_t)st * GB_STAGE);
-                const uint32_t bbase = abase + GB_ASTAGE;
+                const uint32_t d = tbase + (uint32_t)(buf * GB_BN);
+                for (int ks = 0; ks < S; ks++, it++) {
+                    const int st = (int)(it % GB_NS);
+                    if (!gb_wait(&full[st], (uint32_t)(it / GB_NS) & 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t abase = smem_u32(stages + (size_t)st * GB_STAGE);
+                    const uint32_t bbase = abase + GB_ASTAGE;
 #pragma unroll
-                for (int kk = 0; kk < GB_BK / 16; kk++)
-                    gb_mma(tbase, gb_desc(abase + 32u * kk), gb_desc(bbase + 32u * kk), (s | kk) != 0);
-                gb_commit(&empty[st]);  // the stage is free once these MMAs have read it
+                    for (int kk = 0; kk < GB_BK / 16; kk++)
+                        gb_mma(d, gb_desc(abase + 32u * kk), gb_desc(bbase + 32u * kk), (ks | kk) != 0);
+                    gb_commit(&empty[st]);  // the stage is free once these MMAs have read it
+                }
+                gb_commit(&accf[buf]);  // the tile's accumulator is complete once its MMAs are
             }
             gb_commit(done);  // completes once every MMA issued above has finished
             if (!mbar_wait_suspend(done, 0)) atomicOr(&g_gemm_status, 2u);
@@ -183,14 +218,17 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
         // ---------------------------------------------------------------- epilogue
         // warp w reads tensor-memory lanes 32 (w % 4) .. + 31: output rows m0 + 32 (w % 4) + lane
         const int qd = warp & 3;
-        bool ok = mbar_wait_suspend(done, 0);
-        if (!ok) atomicOr(&g_gemm_status, 2u);
-        ok = __all_sync(0xffffffffu, ok && !*abort) != 0;
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const int row = m0 + 32 * qd + lane;
-        const uint32_t tq = tbase + ((uint32_t)(32 * qd) << 16);
         const bool vec = (n & 7) == 0;
-        if (ok) {
+        int ti = 0;
+        for (int id = blockIdx.x; id < ntiles; id += G, ti++) {
+            const int buf = ti & 1;
+            bool ok = gb_wait(&accf[buf], (uint32_t)(ti >> 1) & 1u, abort);
+            ok = __all_sync(0xffffffffu, ok && !*abort) != 0;
+            if (!ok) break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const int m0 = tile_m0(id), n0 = tile_n0(id);
+            const int row = m0 + 32 * qd + lane;
+            const uint32_t tq = tbase + ((uint32_t)(32 * qd) << 16) + (uint32_t)(buf * GB_BN);
 #pragma unroll 1
             for (int c = 0; c < GB_BN / 32; c++) {
                 const int col0 = n0 + 32 * c;
@@ -219,6 +257,10 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
                     }
                 }
             }
+            // the buffer's reads are complete (tcgen05.ld waited): hand it back to the MMA warp
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[buf]);
         }
     }
 
@@ -264,8 +306,12 @@ extern "C" int dense_gemm_bf16(const uint16_t* a, const uint16_t* w, uint16_t* o
     int st = cached_tmap_2d_u8(&ma, a, (uint64_t)k * 2, m, (uint64_t)k * 2, 128, GB_BM, true, who);
     if (st) return st;
     if ((st = cached_tmap_2d_u8(&mw, w, (uint64_t)k * 2, n, (uint64_t)k * 2, 128, GB_BN, true, who))) return st;
-    const int ntm = (int)((m + GB_BM - 1) / GB_BM), ntn = (int)((n + GB_BN - 1) / GB_BN);
-    gemm_bf16_tc_kernel<<<(unsigned)(ntm * ntn), GB_THREADS, GB_SMEM, (cudaStream_t)stream>>>(ma, mw, out, (int)m, (int)n,
-                                                                                             (int)k, ntm);
+    const uint64_t ntiles64 = (uint64_t)((m + GB_BM - 1) / GB_BM) * ((n + GB_BN - 1) / GB_BN);
+    if (ntiles64 >= (1ull << 31)) return fail(BQ_ERR_INVALID, "%s: too many output tiles", who);
+    const int ntm = (int)((m + GB_BM - 1) / GB_BM);
+    const int ntiles = (int)ntiles64;
+    const int grid = ntiles < sm_count() ? ntiles : sm_count();  // persistent: one CTA per SM
+    gemm_bf16_tc_kernel<<<(unsigned)grid, GB_THREADS, GB_SMEM, (cudaStream_t)stream>>>(ma, mw, out, (int)m, (int)n,
+                                                                                       (int)k, ntm, ntiles);
     return check_launch(who);
 }
