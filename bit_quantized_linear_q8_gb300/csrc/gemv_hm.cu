@@ -380,11 +380,15 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
 
     // activations: all M rows at once.  Pass 1 takes each row's maximum |x| (a warp's 32
     // consecutive vectors fall in at most two rows); pass 2 writes the FP16 fragment table,
-    // from registers when every vector fitted in one load batch, else reloading.
+    // from registers when every vector fitted in one load batch, else reloading.  A vector's
+    // row v / kv is a multiply-high by ceil(2^32 / kv): exact while v (ceil(2^32 / kv) kv -
+    // 2^32) < 2^32, i.e. for every v < 8 kv when kv < 23170 (the host keeps k below that).
     constexpr int XV = 8;  // vectors of 8 values per thread and batch
     constexpr int NCT = HM_CWARPS * 32;
     const int kv = k >> 3;     // 8-value vectors per row
     const int tv = M * kv;     // vectors of x
+    const uint32_t kmag = 0xFFFFFFFFu / (uint32_t)kv + 1u;
+    auto row_of = [&](int v) { return (int)__umulhi((uint32_t)v, kmag); };
     const uint4* xv = reinterpret_cast<const uint4*>(p.x);
     uint4 q[XV];
     for (int v0 = 0; v0 < tv; v0 += XV * NCT) {
@@ -402,9 +406,9 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
 #pragma unroll
             for (int h = 0; h < 4; h++)
                 mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(u[h] << 16)), fabsf(__uint_as_float(u[h] & 0xFFFF0000u))));
-            const int j0 = vw / kv;
+            const int j0 = row_of(vw);
             const int v = vw + lane;
-            const bool second = v < tv && v / kv != j0;  // lanes in the row after j0
+            const bool second = v < tv && row_of(v) != j0;  // lanes in the row after j0
             float ma = second ? 0.f : mx, mb = second ? mx : 0.f;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
@@ -436,27 +440,27 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
         for (int e = 0; e < XV; e++) {
             const int v = v0 + e * NCT + tid;
             if (v >= tv) continue;
-            const int j = v / kv, col = (v - j * kv) << 3;
-            // 2^s with the row maximum in [2^14, 2^15); capped where 2^s and 2^-s stay normal
+            const int j = row_of(v), col = (v - j * kv) << 3;
+            const int pb = col >> 7, i = (col >> 5) & 3, tt = (col >> 3) & 3;
+            // 2^s 4^-i, 2^s putting the row maximum in [2^14, 2^15) (capped where 2^s and 2^-s
+            // stay normal): one exact power-of-two product per value
             const uint32_t mb = rowmax[j];
             int sh = mb ? 14 - (int)((mb >> 23) & 0xFF) + 127 : 0;
             sh = max(-113, min(sh, 120));
-            const float p2s = __int_as_float((127 + sh) << 23);
+            const float sc = __int_as_float((127 + sh - 2 * i) << 23);
             const uint32_t u[4] = {q[e].x, q[e].y, q[e].z, q[e].w};
             float X[8];
 #pragma unroll
             for (int h = 0; h < 4; h++) {
-                X[2 * h] = __uint_as_float(u[h] << 16) * p2s;
-                X[2 * h + 1] = __uint_as_float(u[h] & 0xFFFF0000u) * p2s;
+                X[2 * h] = __uint_as_float(u[h] << 16) * sc;
+                X[2 * h + 1] = __uint_as_float(u[h] & 0xFFFF0000u) * sc;
             }
-            const int pb = col >> 7, i = (col >> 5) & 3, tt = (col >> 3) & 3;
-            const float q4 = __int_as_float((127 - 2 * i) << 23);  // 4^-i
 #pragma unroll
             for (int s = 0; s < 2; s++) {
                 const float* e4 = X + 4 * s;
                 // lane (j, tt)'s fragment for MMA 4s + i (columns 0, 2 then 1, 3 of the four),
                 // in quad (4s + i) / 2 at half (4s + i) % 2
-                const uint2 ent = make_uint2(f16x2_bits(e4[0] * q4, e4[2] * q4), f16x2_bits(e4[1] * q4, e4[3] * q4));
+                const uint2 ent = make_uint2(f16x2_bits(e4[0], e4[2]), f16x2_bits(e4[1], e4[3]));
                 const int quad = 2 * s + (i >> 1);
                 *reinterpret_cast<uint2*>(btab + ((((size_t)pb * 4 + quad) * M + j) * 4 + tt) * 16 + (i & 1) * 8) = ent;
             }
@@ -614,7 +618,7 @@ static int hm_plan(int m, int n, int k, int group, int nw, int sms, HmParams* pr
 
 // Shapes this kernel takes: its shared-memory carve-up fits one SM.
 bool gemv_hm_supported(const bq_q2_weight* w, uint32_t m) {
-    if (w->k == 0 || w->n == 0 || m < 1 || m > 8) return false;
+    if (w->k == 0 || w->n == 0 || m < 1 || m > 8 || w->k / 8 >= 23170) return false;
     HmParams prm;
     size_t smem = 0;
     hm_plan((int)m, (int)w->n, (int)w->k, (int)w->group, 1, sm_count(), &prm, &smem);
@@ -623,7 +627,7 @@ bool gemv_hm_supported(const bq_q2_weight* w, uint32_t m) {
 
 // The dual form for an FFN's gate and up weights (the caller has checked that they match).
 bool gemv_hm_dual_supported(const bq_q2_weight* gate, uint32_t m) {
-    if (gate->k == 0 || gate->n == 0 || m < 1 || m > 8) return false;
+    if (gate->k == 0 || gate->n == 0 || m < 1 || m > 8 || gate->k / 8 >= 23170) return false;
     HmParams prm;
     size_t smem = 0;
     hm_plan((int)m, (int)gate->n, (int)gate->k, (int)gate->group, 2, sm_count(), &prm, &smem);
