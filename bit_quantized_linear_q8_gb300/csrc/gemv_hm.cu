@@ -80,6 +80,11 @@ struct HmParams {
     int tmax;                // tiles of the largest CTA
     int tgb;                 // tiles per row group: each TMA box is 128 bytes x 16 tgb rows
     int nstages;
+    // launch constants from the host, so that the CTA's prologue does no division
+    uint32_t ring, btab, scal, scal_w, slot, misc;  // shared-memory offsets (HmLayout)
+    int G;                   // scale groups per row, k / group
+    int lw;                  // log2 of the warps per tile pair (hm_parts)
+    uint32_t kmag;           // ceil(2^32 / (k / 8)): a vector's activation row by a multiply-high
 };
 
 // Warps sharing a tile pair (each takes 1/parts of a chunk's pack blocks), from the tile
@@ -260,7 +265,7 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);  // the swizzled boxes need 1024-byte alignment
     const int n = p.n, k = p.k;
-    const HmLayout L(M, k, p.group, p.tgb, p.nstages, p.tmax, NW);
+    const HmParams& L = p;  // the shared-memory offsets
     uint8_t* ring = smem + L.ring;
     uint8_t* btab = smem + L.btab;
     uint8_t* scal = smem + L.scal;
@@ -274,11 +279,12 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ntiles = (n + 15) >> 4;
-    const int t0 = (int)((int64_t)blockIdx.x * ntiles / gridDim.x);
-    const int TC = (int)((int64_t)(blockIdx.x + 1) * ntiles / gridDim.x) - t0;  // the CTA's tiles
+    // (32-bit: the host keeps tiles x CTAs below 2^31)
+    const int t0 = (int)((blockIdx.x * (uint32_t)ntiles) / gridDim.x);
+    const int TC = (int)(((blockIdx.x + 1) * (uint32_t)ntiles) / gridDim.x) - t0;  // the CTA's tiles
     const int r0 = 16 * t0;
     const int R = min(16 * TC, n - r0);  // the CTA's rows
-    const int P = k >> 7, G = k / p.group;
+    const int P = k >> 7, G = p.G;
     const int kb = k >> 2;  // code bytes per row
     const int NST = p.nstages, TGB = p.tgb;
     const int ngrp = (TC + TGB - 1) / TGB;      // row groups
@@ -387,7 +393,7 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
     constexpr int NCT = HM_CWARPS * 32;
     const int kv = k >> 3;     // 8-value vectors per row
     const int tv = M * kv;     // vectors of x
-    const uint32_t kmag = 0xFFFFFFFFu / (uint32_t)kv + 1u;
+    const uint32_t kmag = p.kmag;
     auto row_of = [&](int v) { return (int)__umulhi((uint32_t)v, kmag); };
     const uint4* xv = reinterpret_cast<const uint4*>(p.x);
     uint4 q[XV];
@@ -477,9 +483,9 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
     const int gsh = __ffs(p.group) - 1 - 7;  // group = 128 << gsh
     const uint16_t* srow = reinterpret_cast<const uint16_t*>(scal + ((int64_t)r0 * G * 2 - s_lo));
     const int tlast = TC - (ngrp - 1) * TGB;  // tiles of the last row group
-    const int wpp = hm_parts(TGB, NW);  // warps per tile pair (a power of two)
-    const int pair = warp / wpp, part = warp - pair * wpp;
-    const int nbw = 8 / wpp > 0 ? 8 / wpp : 1;  // pack blocks per chunk and warp
+    const int wpp = 1 << p.lw;  // warps per tile pair (a power of two, at most 8)
+    const int pair = warp >> p.lw, part = warp & (wpp - 1);
+    const int nbw = 8 >> p.lw;  // pack blocks per chunk and warp
     const int jb = min(g, M - 1);  // activation row of the lane's B fragments (columns >= M are never stored)
     const size_t pstride = (size_t)16 * p.tmax * M;  // one part's (and weight's) partial sums
     // second tile of a pair: the next tile of the box, or the same tile of the up weight
@@ -619,6 +625,7 @@ static int hm_plan(int m, int n, int k, int group, int nw, int sms, HmParams* pr
 // Shapes this kernel takes: its shared-memory carve-up fits one SM.
 bool gemv_hm_supported(const bq_q2_weight* w, uint32_t m) {
     if (w->k == 0 || w->n == 0 || m < 1 || m > 8 || w->k / 8 >= 23170) return false;
+    if ((uint64_t)((w->n + 15) / 16) * (uint64_t)sm_count() >= (1ull << 31)) return false;
     HmParams prm;
     size_t smem = 0;
     hm_plan((int)m, (int)w->n, (int)w->k, (int)w->group, 1, sm_count(), &prm, &smem);
@@ -628,6 +635,7 @@ bool gemv_hm_supported(const bq_q2_weight* w, uint32_t m) {
 // The dual form for an FFN's gate and up weights (the caller has checked that they match).
 bool gemv_hm_dual_supported(const bq_q2_weight* gate, uint32_t m) {
     if (gate->k == 0 || gate->n == 0 || m < 1 || m > 8 || gate->k / 8 >= 23170) return false;
+    if ((uint64_t)((gate->n + 15) / 16) * (uint64_t)sm_count() >= (1ull << 31)) return false;
     HmParams prm;
     size_t smem = 0;
     hm_plan((int)m, (int)gate->n, (int)gate->k, (int)gate->group, 2, sm_count(), &prm, &smem);
@@ -677,6 +685,19 @@ static int launch_hm(const uint16_t* x, const bq_q2_weight* w, const bq_q2_weigh
     tmap2 = tmap;
     if (dual && (st = cached_tmap_2d_u8(&tmap2, w2->data, w2->k / 4, w2->n, w2->k / 4, 128, 16 * prm.tgb, true, who)))
         return st;
+    {
+        const HmLayout L(m, (int)w->k, (int)w->group, prm.tgb, prm.nstages, prm.tmax, dual ? 2 : 1);
+        prm.ring = (uint32_t)L.ring;
+        prm.btab = (uint32_t)L.btab;
+        prm.scal = (uint32_t)L.scal;
+        prm.scal_w = (uint32_t)L.scal_w;
+        prm.slot = (uint32_t)L.slot;
+        prm.misc = (uint32_t)L.misc;
+        prm.G = (int)(w->k / w->group);
+        const int wpp = hm_parts(prm.tgb, dual ? 2 : 1);
+        prm.lw = wpp == 8 ? 3 : wpp == 4 ? 2 : wpp == 2 ? 1 : 0;
+        prm.kmag = 0xFFFFFFFFu / (w->k / 8) + 1u;
+    }
     prm.codes = (const uint8_t*)w->data;
     prm.scales = (const uint16_t*)((const uint8_t*)w->data + (size_t)w->n * (w->k / 4));
     prm.codes2 = dual ? (const uint8_t*)w2->data : nullptr;
