@@ -85,7 +85,13 @@ struct HmParams {
     int G;                   // scale groups per row, k / group
     int lw;                  // log2 of the warps per tile pair (hm_parts)
     uint32_t kmag;           // ceil(2^32 / (k / 8)): a vector's activation row by a multiply-high
+    uint32_t cmag;           // ceil(2^32 / CTAs): the CTA's tile range by a multiply-high
+    uint32_t gmag;           // ceil(2^32 / tgb): the CTA's row groups by a multiply-high
 };
+
+// x / d by a multiply-high with mag = ceil(2^32 / d) computed in 32 bits, which wraps to 0
+// exactly when d = 1.
+__device__ __forceinline__ uint32_t hm_div(uint32_t x, uint32_t mag) { return mag ? __umulhi(x, mag) : x; }
 
 // Warps sharing a tile pair (each takes 1/parts of a chunk's pack blocks), from the tile
 // pairs per row group: tgb / 2 rounded up, or tgb in the dual (nw = 2) form.
@@ -279,15 +285,16 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ntiles = (n + 15) >> 4;
-    // (32-bit: the host keeps tiles x CTAs below 2^31)
-    const int t0 = (int)((blockIdx.x * (uint32_t)ntiles) / gridDim.x);
-    const int TC = (int)(((blockIdx.x + 1) * (uint32_t)ntiles) / gridDim.x) - t0;  // the CTA's tiles
+    // tile range [c T / C, (c + 1) T / C) by multiply-highs (exact: the host keeps T C C below
+    // 2^32, so c T (ceil(2^32 / C) C - 2^32) < 2^32)
+    const int t0 = (int)hm_div(blockIdx.x * (uint32_t)ntiles, p.cmag);
+    const int TC = (int)hm_div((blockIdx.x + 1) * (uint32_t)ntiles, p.cmag) - t0;  // the CTA's tiles
     const int r0 = 16 * t0;
     const int R = min(16 * TC, n - r0);  // the CTA's rows
     const int P = k >> 7, G = p.G;
     const int kb = k >> 2;  // code bytes per row
     const int NST = p.nstages, TGB = p.tgb;
-    const int ngrp = (TC + TGB - 1) / TGB;      // row groups
+    const int ngrp = (int)hm_div((uint32_t)(TC + TGB - 1), p.gmag);  // row groups
     const int nkc = (P + 7) >> 3;               // 1024-column chunks per row group
     const int nch = ngrp * nkc;
     const uint32_t box_bytes = (uint32_t)TGB * HM_BOX;
@@ -303,16 +310,17 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
     if (s_hi > plane16) s_hi = plane16;
     if (s_hi < s_lo) s_hi = s_lo;
 
-    if (tid == 0) {
-        for (int s = 0; s < NST; s++) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], HM_CWARPS);
-        }
+    if (tid < NST) {
+        mbar_init(&full[tid], 1);
+        mbar_init(&empty[tid], HM_CWARPS);
+        fence_barrier_init();
+    }
+    if (tid == 64) {
         mbar_init(sbar, 1);
         mbar_init(xready, 1);
         fence_barrier_init();
     }
-    if (tid < 8) rowmax[tid] = 0u;
+    if (tid >= 96 && tid < 104) rowmax[tid - 96] = 0u;
     if (tid == 32)
         for (int w = 0; w < NW; w++) {
             const uint8_t* sp = w ? reinterpret_cast<const uint8_t*>(p.scales2) : splane;
@@ -384,8 +392,8 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
     pdl_wait();
     pdl_launch_dependents();
 
-    // activations: all M rows at once.  Pass 1 takes each row's maximum |x| (a warp's 32
-    // consecutive vectors fall in at most two rows); pass 2 writes the FP16 fragment table,
+    // activations: all M rows at once.  Pass 1 takes each row's maximum |x| (per thread and
+    // row in registers, then one warp reduction per row); pass 2 writes the FP16 fragment table,
     // from registers when every vector fitted in one load batch, else reloading.  A vector's
     // row v / kv is a multiply-high by ceil(2^32 / kv): exact while v (ceil(2^32 / kv) kv -
     // 2^32) < 2^32, i.e. for every v < 8 kv when kv < 23170 (the host keeps k below that).
@@ -397,6 +405,9 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
     auto row_of = [&](int v) { return (int)__umulhi((uint32_t)v, kmag); };
     const uint4* xv = reinterpret_cast<const uint4*>(p.x);
     uint4 q[XV];
+    float rmx[M];
+#pragma unroll
+    for (int jj = 0; jj < M; jj++) rmx[jj] = 0.f;
     for (int v0 = 0; v0 < tv; v0 += XV * NCT) {
 #pragma unroll
         for (int e = 0; e < XV; e++) {
@@ -405,26 +416,24 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
         }
 #pragma unroll
         for (int e = 0; e < XV; e++) {
-            const int vw = v0 + e * NCT + warp * 32;  // the warp's first vector
-            if (vw >= tv) break;
+            const int v = v0 + e * NCT + tid;
+            if (v >= tv) continue;
             const uint32_t u[4] = {q[e].x, q[e].y, q[e].z, q[e].w};
             float mx = 0.f;
 #pragma unroll
             for (int h = 0; h < 4; h++)
                 mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(u[h] << 16)), fabsf(__uint_as_float(u[h] & 0xFFFF0000u))));
-            const int j0 = row_of(vw);
-            const int v = vw + lane;
-            const bool second = v < tv && row_of(v) != j0;  // lanes in the row after j0
-            float ma = second ? 0.f : mx, mb = second ? mx : 0.f;
+            const int j = row_of(v);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, o));
-                mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
-            }
-            const bool has_second = __any_sync(0xffffffffu, second);
-            if (lane == 0) atomicMax(&rowmax[j0], __float_as_uint(ma));
-            if (lane == 0 && has_second) atomicMax(&rowmax[j0 + 1], __float_as_uint(mb));
+            for (int jj = 0; jj < M; jj++) rmx[jj] = j == jj ? fmaxf(rmx[jj], mx) : rmx[jj];
         }
+    }
+#pragma unroll
+    for (int jj = 0; jj < M; jj++) {
+        float r = rmx[jj];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) r = fmaxf(r, __shfl_xor_sync(0xffffffffu, r, o));
+        if (lane == 0 && r > 0.f) atomicMax(&rowmax[jj], __float_as_uint(r));
     }
     consumer_sync();
     if (tid == 0) mbar_arrive(xready);
@@ -625,7 +634,7 @@ static int hm_plan(int m, int n, int k, int group, int nw, int sms, HmParams* pr
 // Shapes this kernel takes: its shared-memory carve-up fits one SM.
 bool gemv_hm_supported(const bq_q2_weight* w, uint32_t m) {
     if (w->k == 0 || w->n == 0 || m < 1 || m > 8 || w->k / 8 >= 23170) return false;
-    if ((uint64_t)((w->n + 15) / 16) * (uint64_t)sm_count() >= (1ull << 31)) return false;
+    if ((uint64_t)((w->n + 15) / 16) * (uint64_t)sm_count() * (uint64_t)sm_count() >= (1ull << 32)) return false;
     HmParams prm;
     size_t smem = 0;
     hm_plan((int)m, (int)w->n, (int)w->k, (int)w->group, 1, sm_count(), &prm, &smem);
@@ -635,7 +644,7 @@ bool gemv_hm_supported(const bq_q2_weight* w, uint32_t m) {
 // The dual form for an FFN's gate and up weights (the caller has checked that they match).
 bool gemv_hm_dual_supported(const bq_q2_weight* gate, uint32_t m) {
     if (gate->k == 0 || gate->n == 0 || m < 1 || m > 8 || gate->k / 8 >= 23170) return false;
-    if ((uint64_t)((gate->n + 15) / 16) * (uint64_t)sm_count() >= (1ull << 31)) return false;
+    if ((uint64_t)((gate->n + 15) / 16) * (uint64_t)sm_count() * (uint64_t)sm_count() >= (1ull << 32)) return false;
     HmParams prm;
     size_t smem = 0;
     hm_plan((int)m, (int)gate->n, (int)gate->k, (int)gate->group, 2, sm_count(), &prm, &smem);
@@ -697,6 +706,8 @@ static int launch_hm(const uint16_t* x, const bq_q2_weight* w, const bq_q2_weigh
         const int wpp = hm_parts(prm.tgb, dual ? 2 : 1);
         prm.lw = wpp == 8 ? 3 : wpp == 4 ? 2 : wpp == 2 ? 1 : 0;
         prm.kmag = 0xFFFFFFFFu / (w->k / 8) + 1u;
+        prm.cmag = 0xFFFFFFFFu / (uint32_t)ncta + 1u;
+        prm.gmag = 0xFFFFFFFFu / (uint32_t)prm.tgb + 1u;
     }
     prm.codes = (const uint8_t*)w->data;
     prm.scales = (const uint16_t*)((const uint8_t*)w->data + (size_t)w->n * (w->k / 4));
