@@ -449,6 +449,19 @@ def test_dense_gemm_bf16_small(B, m, n, k):
     check_bf16_vs_f64(y, O.gemm_bf16(a, w), "dense gemm m=%d n=%d k=%d" % (m, n, k))
 
 
+@pytest.mark.parametrize("m,n,k", [(300, 20000, 128), (129, 39000, 64)])
+def test_dense_gemm_bf16_persistent(B, m, n, k):
+    """More output tiles than SMs, so every CTA walks several tiles through both tensor-memory
+    accumulators (237 and 306 tiles of 128 x 256), with ragged last m and n tiles; every
+    element against the oracle."""
+    g = synth._gen(1400 + m + n + k)
+    a = synth.activations(g, m, k)
+    w = synth.dense_weight(g, n, k)
+    y = bf16_dev_to_u16(B.dense_gemm_bf16(to_dev_u16_as_bf16(a), to_dev_u16_as_bf16(w)))
+    check_bf16_vs_f64(y, O.gemm_bf16(a, w), "dense gemm m=%d n=%d k=%d" % (m, n, k))
+    assert B.lib().bq_device_status() == 0
+
+
 def test_dense_gemm_bf16_edges(B):
     import torch
     a = torch.zeros((4, 64), dtype=torch.bfloat16, device="cuda")
