@@ -640,11 +640,13 @@ int ffn_q2_km(const uint16_t* x, const bq_q2_weight* gate, const bq_q2_weight* u
         // the up projection's epilogue also forms h = SiLU(g) * u in gate_scratch
         if ((st = launch_q2_gemv(x, up, up_scratch, m, s, who, gate_scratch))) return st;
     }
-    // The down projection runs without the cluster K split here: right after the up
-    // projection a cluster launch loses its early start (measured: chain 54.9 us with the
-    // split against 48.0 us without at m = 2, equal at m = 3), while on its own the split
-    // GEMV is the faster one (13.5 against 20.8 us).
-    return launch_q2_gemv(gate_scratch, down, out, m, s, who, nullptr, false);
+    // The down projection: the FP16 warp-MMA kernel where its activation table fits one SM
+    // (k = 17408: m <= 4), without the cluster K split of the older kernel (right after the
+    // gate/up launch a cluster launch loses its early start: chain 42.8 against 36.7 us at
+    // m = 2); where the table does not fit, the older kernel with its cluster K split (chain
+    // 50.2 against 57.2 us unsplit at m = 8).
+    if (gemv_hm_supported(down, m)) return launch_q2_gemv(gate_scratch, down, out, m, s, who, nullptr, false);
+    return launch_q2_gemv_mma(gate_scratch, down, out, m, nullptr, true, s, who);
 }
 
 }  // extern "C"
