@@ -276,6 +276,276 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
 
 using namespace bq8;
 
+// ---------------------------------------------------------------------------------------
+// The CTA-pair form (m > 128): a cluster of two CTAs computes a 256 x 256 output tile with
+// tcgen05.mma.cta_group::2 M256 N256 K16, issued by the even CTA.  CTA r of the pair holds
+// rows 128 r .. 128 r + 127 of the tile's activations and of its weight rows (the MMA's B
+// operand is split along N across the pair), both at the same shared-memory offsets, and
+// receives its 128 output rows x 256 columns in its own tensor memory.  Per K step each CTA
+// stages 16 KB + 16 KB instead of 16 + 32 KB for a 128 x 256 tile, so the operand traffic
+// through each SM's shared memory per MMA is a third lower.
+//  * Each CTA's producer lane streams its own halves through a six-stage ring; both CTAs' copies
+//    complete their bytes on the even CTA's `full` barrier (the cta_group::2 form of the TMA
+//    load), whose one arrival expects the pair's 64 KB per stage.
+//  * The even CTA's MMA lane commits each K step to the `empty` barriers of both CTAs and each
+//    tile's last step to both CTAs' accumulator barriers (multicast commits); both CTAs'
+//    epilogue warps read their lanes and arrive (the odd CTA's remotely) on the even CTA's
+//    accumulator-empty barrier, which counts eight warps.
+//  * Tensor memory is allocated and freed for the pair (cta_group::2, one warp in each CTA).
+//  * Every wait is bounded; both CTAs reach the final cluster barrier on every path.
+constexpr int GP_BM = 128;                              // rows per CTA (256 per pair)
+constexpr int GP_BN = 256;                              // output columns per pair tile
+constexpr int GP_NS = 6;
+constexpr uint32_t GP_ASTAGE = GP_BM * GB_BK * 2;      // 16 KB
+constexpr uint32_t GP_BSTAGE = (GP_BN / 2) * GB_BK * 2;  // 16 KB: this CTA's half of the weight rows
+constexpr uint32_t GP_STAGE = GP_ASTAGE + GP_BSTAGE;
+constexpr size_t GP_SMEM = 1024 + (size_t)GP_NS * GP_STAGE + (2 * GP_NS + 5) * 8 + 16;
+static_assert(GP_SMEM <= 227 * 1024, "shared memory budget");
+// D fp32, A and B BF16, both K-major, N = 256, M = 256 (the pair)
+constexpr uint32_t GP_IDESC =
+    (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(GP_BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+
+__device__ __forceinline__ uint32_t gp_cluster_addr(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void gp_arrive_cluster(uint32_t addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+// 2-D TMA tile load into this CTA's shared memory whose bytes complete on `bar_cluster`, a
+// barrier of either CTA of the pair (shared::cluster address).
+__device__ __forceinline__ void gp_tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
+}
+__device__ __forceinline__ void gp_cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void gp_commit_pair(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"((uint16_t)3)
+        : "memory");
+}
+__device__ __forceinline__ bool gp_try_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, "
+        "p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// Bounded wait with cluster-scope acquire (for barriers that receive remote arrivals).
+__device__ __forceinline__ bool gp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    for (uint32_t it = 0; it < GB_WAIT_LIMIT; it++) {
+        if (gp_try_cluster(bar, parity)) return true;
+        if (*abort) return false;
+    }
+    *abort = 1;
+    atomicOr(&g_gemm_status, 1u);
+    return false;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GB_THREADS, 1)
+    gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapW,
+                          uint16_t* __restrict__ out, int m, int n, int k, int ntm, int ntiles) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* stages = align1024(smem_raw);  // [stage][a 128 x 64 | w 128 x 64] BF16, 128-byte swizzle
+    uint64_t* full = reinterpret_cast<uint64_t*>(stages + GP_NS * GP_STAGE);
+    uint64_t* empty = full + GP_NS;
+    uint64_t* accf = empty + GP_NS;  // [2] accumulator buffer holds a finished tile (both CTAs)
+    uint64_t* acce = accf + 2;       // [2] both CTAs' epilogues have read the buffer (even CTA)
+    uint64_t* done = acce + 2;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
+
+    uint32_t rank;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int S = k / GB_BK;
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    auto tile_m0 = [&](int id) { return (id % ntm) * (2 * GP_BM); };
+    auto tile_n0 = [&](int id) { return (id / ntm) * GP_BN; };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < GP_NS; s++) {
+            mbar_init(&full[s], 1);  // the even CTA's: one arrival expecting both CTAs' bytes
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&accf[b], 1);
+            mbar_init(&acce[b], 8);  // four epilogue warps in each CTA (used on the even CTA)
+        }
+        mbar_init(done, 1);
+        *abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                     "n"(GB_TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    gp_cluster_sync();  // both CTAs' barriers exist before any remote arrive or MMA
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tbase = *tslot;
+
+    if (warp == 1) {
+        // ---------------------------------------------------------------- TMA producer (each CTA)
+        if (lane == 0) {
+            int64_t it = 0;
+            bool ok = true;
+            for (int id = pair; id < ntiles && ok; id += npairs) {
+                const int ma0 = tile_m0(id) + GP_BM * (int)rank, nb0 = tile_n0(id) + (GP_BN / 2) * (int)rank;
+                for (int ks = 0; ks < S; ks++, it++) {
+                    const int st = (int)(it % GP_NS);
+                    // the stage is free in both CTAs once the pair's MMAs of step it - NS have read it
+                    if (it >= GP_NS && !gb_wait(&empty[st], (uint32_t)((it / GP_NS) - 1) & 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* dst = stages + (size_t)st * GP_STAGE;
+                    const uint32_t bar = gp_cluster_addr(&full[st], 0);
+                    if (rank == 0) mbar_arrive_expect_tx(&full[st], 2 * GP_STAGE);
+                    gp_tma_load_2d(dst, &mapA, ks * GB_BK * 2, ma0, bar);
+                    gp_tma_load_2d(dst + GP_ASTAGE, &mapW, ks * GB_BK * 2, nb0, bar);
+                }
+            }
+            // wind down (even CTA): the last copies of both CTAs land before the pair passes its
+            // final cluster barrier
+            if (rank == 0)
+                for (int64_t j = it > GP_NS ? it - GP_NS : 0; j < it; j++)
+                    if (!mbar_wait_suspend(&full[j % GP_NS], (uint32_t)(j / GP_NS) & 1u)) atomicOr(&g_gemm_status, 2u);
+        }
+        __syncwarp();
+    } else if (warp == 0 && rank == 0) {
+        // ---------------------------------------------------------------- MMA issuer (even CTA)
+        if (lane == 0) {
+            int64_t it = 0;
+            bool ok = true;
+            int ti = 0;
+            for (int id = pair; id < ntiles && ok; id += npairs, ti++) {
+                const int buf = ti & 1;
+                if (ti >= 2 && !gp_wait(&acce[buf], (uint32_t)((ti >> 1) - 1) & 1u, abort)) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t d = tbase + (uint32_t)(buf * GP_BN);
+                for (int ks = 0; ks < S; ks++, it++) {
+                    const int st = (int)(it % GP_NS);
+                    if (!gb_wait(&full[st], (uint32_t)(it / GP_NS) & 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t abase = smem_u32(stages + (size_t)st * GP_STAGE);
+                    const uint32_t bbase = abase + GP_ASTAGE;
+#pragma unroll
+                    for (int kk = 0; kk < GB_BK / 16; kk++)
+                        asm volatile(
+                            "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
+                            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+                            "l"(gb_desc(abase + 32u * kk)), "l"(gb_desc(bbase + 32u * kk)), "r"(GP_IDESC),
+                            "r"((uint32_t)(ks | kk)));
+                    gp_commit_pair(&empty[st]);  // both CTAs' stage is free once these MMAs have read it
+                }
+                gp_commit_pair(&accf[buf]);  // both CTAs' accumulator rows are complete
+            }
+            gp_commit_pair(done);  // completes once every MMA issued above has finished
+            if (!mbar_wait_suspend(done, 0)) atomicOr(&g_gemm_status, 2u);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------------- epilogue (each CTA)
+        // warp w reads tensor-memory lanes 32 (w % 4) .. + 31: output rows m0 + 128 rank + 32 (w % 4) + lane
+        const int qd = warp & 3;
+        const bool vec = (n & 7) == 0;
+        const uint32_t acce_addr0 = gp_cluster_addr(&acce[0], 0), acce_addr1 = gp_cluster_addr(&acce[1], 0);
+        int ti = 0;
+        for (int id = pair; id < ntiles; id += npairs, ti++) {
+            const int buf = ti & 1;
+            bool ok = gb_wait(&accf[buf], (uint32_t)(ti >> 1) & 1u, abort);
+            ok = __all_sync(0xffffffffu, ok && !*abort) != 0;
+            if (!ok) break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const int m0 = tile_m0(id) + GP_BM * (int)rank, n0 = tile_n0(id);
+            const int row = m0 + 32 * qd + lane;
+            const uint32_t tq = tbase + ((uint32_t)(32 * qd) << 16) + (uint32_t)(buf * GP_BN);
+#pragma unroll 1
+            for (int c = 0; c < GP_BN / 32; c++) {
+                const int col0 = n0 + 32 * c;
+                if (col0 >= n) break;  // warp-uniform
+                uint32_t v[32];
+                gb_ld32(tq + 32u * c, v);
+                if (row >= m) continue;
+                uint16_t* dst = out + (size_t)row * n + col0;
+                if (vec && col0 + 32 <= n) {
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        uint4 o;
+                        o.x = bf162_bits(__floats2bfloat162_rn(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])));
+                        o.y = bf162_bits(__floats2bfloat162_rn(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])));
+                        o.z = bf162_bits(__floats2bfloat162_rn(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])));
+                        o.w = bf162_bits(__floats2bfloat162_rn(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+                        *reinterpret_cast<uint4*>(dst + 8 * q) = o;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; e++) {
+                        if (col0 + e < n) {
+                            const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(v[e]));
+                            dst[e] = *reinterpret_cast<const uint16_t*>(&b);
+                        }
+                    }
+                }
+            }
+            // this warp's reads of the buffer are complete: tell the even CTA's MMA lane
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) gp_arrive_cluster(buf ? acce_addr1 : acce_addr0);
+        }
+    }
+
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    gp_cluster_sync();  // no remote arrive or MMA of the pair is outstanding past this point
+    if (warp == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tbase), "n"(GB_TMEM_COLS));
+    }
+}
+
+// The CTA-pair form for m > 128: one pair per two SMs walks the 256 x 256 tiles.
+static int launch_pair(const uint16_t* a, const uint16_t* w, uint16_t* out, uint32_t m, uint32_t n, uint32_t k,
+                       cudaStream_t stream, int dev, const char* who) {
+    static int configured[64] = {};
+    if (!configured[dev]) {
+        if (cudaFuncSetAttribute(gemm_bf16_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GP_SMEM) !=
+            cudaSuccess)
+            return fail(BQ_ERR_LAUNCH, "%s: cannot reserve %zu bytes of shared memory", who, GP_SMEM);
+        configured[dev] = 1;
+    }
+    CUtensorMap ma, mw;
+    int st = cached_tmap_2d_u8(&ma, a, (uint64_t)k * 2, m, (uint64_t)k * 2, 128, GP_BM, true, who);
+    if (st) return st;
+    if ((st = cached_tmap_2d_u8(&mw, w, (uint64_t)k * 2, n, (uint64_t)k * 2, 128, GP_BN / 2, true, who))) return st;
+    const uint64_t ntiles64 = (uint64_t)((m + 2 * GP_BM - 1) / (2 * GP_BM)) * ((n + GP_BN - 1) / GP_BN);
+    if (ntiles64 >= (1ull << 31)) return fail(BQ_ERR_INVALID, "%s: too many output tiles", who);
+    const int ntm = (int)((m + 2 * GP_BM - 1) / (2 * GP_BM));
+    const int ntiles = (int)ntiles64;
+    const int pairs_max = sm_count() / 2;
+    const int npairs = ntiles < pairs_max ? ntiles : pairs_max;
+    gemm_bf16_pair_kernel<<<(unsigned)(2 * npairs), GB_THREADS, GP_SMEM, stream>>>(ma, mw, out, (int)m, (int)n, (int)k,
+                                                                                     ntm, ntiles);
+    return check_launch(who);
+}
+
 extern "C" int dense_gemm_bf16(const uint16_t* a, const uint16_t* w, uint16_t* out, uint32_t m, uint32_t n,
                                uint32_t k, bq_stream_t stream) {
     const char* who = "dense_gemm_bf16";
@@ -295,6 +565,7 @@ extern "C" int dense_gemm_bf16(const uint16_t* a, const uint16_t* w, uint16_t* o
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 64) dev = 63;
+    if (m > (uint32_t)GB_BM) return launch_pair(a, w, out, m, n, k, (cudaStream_t)stream, dev, who);
     if (!configured[dev]) {
         if (cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GB_SMEM) !=
             cudaSuccess)
