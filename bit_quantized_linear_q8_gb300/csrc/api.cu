@@ -146,6 +146,64 @@ int cached_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t row_bytes, ui
     return BQ_OK;
 }
 
+// A byte matrix [rows][row_bytes] (row_bytes a multiple of 128) seen as 128-byte column blocks:
+// dims (128, rows, row_bytes / 128), strides (row_bytes, 128), box (128, box_rows, nblk), 128-byte
+// swizzle.  One request brings nblk column blocks of box_rows rows, laid out [block][row][128 B]
+// in shared memory, the layout of nblk separate 2-D boxes.  Cached like cached_tmap_2d_u8.
+int cached_tmap_chunks_u8(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows,
+                          uint32_t nblk, const char* who) {
+    struct Entry {
+        const void* base;
+        uint64_t row_bytes, rows;
+        uint32_t box_rows, nblk;
+        int dev;
+        bool used;
+        CUtensorMap map;
+    };
+    constexpr int N = 64;
+    static Entry table[N];
+    static int next = 0;
+    static std::mutex mu;
+    if (row_bytes % 128 != 0 || nblk == 0) return fail(BQ_ERR_INVALID, "%s: internal chunk map shape", who);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < N; i++) {
+            const Entry& e = table[i];
+            if (e.used && e.base == base && e.row_bytes == row_bytes && e.rows == rows && e.box_rows == box_rows &&
+                e.nblk == nblk && e.dev == dev) {
+                *map = e.map;
+                return BQ_OK;
+            }
+        }
+    }
+    PFN_encodeTiled fn = encode_fn();
+    if (!fn) return fail(BQ_ERR_UNSUPPORTED, "%s: cuTensorMapEncodeTiled unavailable from the driver", who);
+    const cuuint64_t gd[3] = {128, rows, row_bytes / 128};
+    const cuuint64_t gs[2] = {row_bytes, 128};
+    const cuuint32_t bx[3] = {128, box_rows, nblk};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUtensorMap fresh;
+    CUresult r = fn(&fresh, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), gd, gs, bx, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(BQ_ERR_INVALID, "%s: tensor map encoding failed (CUresult %d)", who, (int)r);
+    std::lock_guard<std::mutex> lock(mu);
+    Entry& e = table[next];
+    next = (next + 1) % N;
+    e.base = base;
+    e.row_bytes = row_bytes;
+    e.rows = rows;
+    e.box_rows = box_rows;
+    e.nblk = nblk;
+    e.dev = dev;
+    e.map = fresh;
+    e.used = true;
+    *map = fresh;
+    return BQ_OK;
+}
+
 int make_tmap_3d_u8(CUtensorMap* map, const void* base, const uint64_t (&dims)[3], const uint64_t (&strides)[2],
                     const uint32_t (&box)[3], const char* who) {
     PFN_encodeTiled fn = encode_fn();

@@ -43,6 +43,10 @@ int cached_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t row_bytes, ui
 
 // 3-D tiled TMA descriptor over bytes: dims {d0, d1, d2}, byte strides of d1 and d2 (any
 // order, multiples of 16), box {b0, b1, b2} (b0 a multiple of 16), no swizzle.
+// A byte matrix [rows][row_bytes] (row_bytes a multiple of 128) as 128-byte column blocks: one
+// request brings nblk blocks of box_rows rows, laid out [block][row][128 B] (api.cu).
+int cached_tmap_chunks_u8(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows,
+                          uint32_t nblk, const char* who);
 int make_tmap_3d_u8(CUtensorMap* map, const void* base, const uint64_t (&dims)[3], const uint64_t (&strides)[2],
                     const uint32_t (&box)[3], const char* who);
 

@@ -87,6 +87,7 @@ struct HmParams {
     uint32_t kmag;           // ceil(2^32 / (k / 8)): a vector's activation row by a multiply-high
     uint32_t cmag;           // ceil(2^32 / CTAs): the CTA's tile range by a multiply-high
     uint32_t gmag;           // ceil(2^32 / tgb): the CTA's row groups by a multiply-high
+    int chunk3d;             // 1: the maps are 3-D chunk maps, one request per weight and chunk
 };
 
 // x / d by a multiply-high with mag = ceil(2^32 / d) computed in 32 bits, which wraps to 0
@@ -354,14 +355,23 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
                     ok = false;
                     break;
                 }
-                // one box of 128 bytes x 16 TGB rows per 512-column half that starts inside the row
                 uint8_t* dst = ring + (size_t)cur.s * stage_bytes;
-                const int nh = cur.kc * 256 + 128 < kb ? 2 : 1;
-                mbar_arrive_expect_tx(&full[cur.s], (uint32_t)(NW * nh) * box_bytes);
-                for (int w = 0; w < NW; w++)
-                    for (int h = 0; h < nh; h++)
-                        tma_load_2d(dst + (size_t)(w * 2 + h) * box_bytes, w ? &tmap2 : &tmap, cur.kc * 256 + h * 128,
-                                    r0 + 16 * cur.gi * TGB, &full[cur.s]);
+                if (p.chunk3d) {
+                    // one request per weight: both 512-column halves (128-byte column blocks 2 kc
+                    // and 2 kc + 1) of 16 TGB rows, the layout of the two 2-D boxes below
+                    mbar_arrive_expect_tx(&full[cur.s], (uint32_t)(NW * 2) * box_bytes);
+                    for (int w = 0; w < NW; w++)
+                        tma_load_3d(dst + (size_t)(w * 2) * box_bytes, w ? &tmap2 : &tmap, 0, r0 + 16 * cur.gi * TGB,
+                                    2 * cur.kc, &full[cur.s]);
+                } else {
+                    // one box of 128 bytes x 16 TGB rows per 512-column half that starts inside the row
+                    const int nh = cur.kc * 256 + 128 < kb ? 2 : 1;
+                    mbar_arrive_expect_tx(&full[cur.s], (uint32_t)(NW * nh) * box_bytes);
+                    for (int w = 0; w < NW; w++)
+                        for (int h = 0; h < nh; h++)
+                            tma_load_2d(dst + (size_t)(w * 2 + h) * box_bytes, w ? &tmap2 : &tmap,
+                                        cur.kc * 256 + h * 128, r0 + 16 * cur.gi * TGB, &full[cur.s]);
+                }
                 nis++;
                 if (c == (NST - 1 > HM_EARLY_CHUNKS ? NST - 1 : HM_EARLY_CHUNKS) && nch > NST) {
                     // the ring is full: the CTA's later row groups into L2, 64 KB per request
@@ -688,12 +698,22 @@ static int launch_hm(const uint16_t* x, const bq_q2_weight* w, const bq_q2_weigh
             return fail(BQ_ERR_LAUNCH, "%s: cannot reserve %zu bytes of shared memory", who, smem);
         configured_smem[dev][dual][m - 1] = (int)smem;
     }
+    // rows of a whole number of 128-byte column blocks (k % 512 == 0): one 3-D request brings a chunk's
+    // two column blocks; otherwise two 2-D boxes per chunk
     CUtensorMap tmap, tmap2;
-    int st = cached_tmap_2d_u8(&tmap, w->data, w->k / 4, w->n, w->k / 4, 128, 16 * prm.tgb, true, who);
-    if (st) return st;
-    tmap2 = tmap;
-    if (dual && (st = cached_tmap_2d_u8(&tmap2, w2->data, w2->k / 4, w2->n, w2->k / 4, 128, 16 * prm.tgb, true, who)))
-        return st;
+    int st;
+    prm.chunk3d = (w->k % 512 == 0) ? 1 : 0;
+    if (prm.chunk3d) {
+        if ((st = cached_tmap_chunks_u8(&tmap, w->data, w->k / 4, w->n, 16 * prm.tgb, 2, who))) return st;
+        tmap2 = tmap;
+        if (dual && (st = cached_tmap_chunks_u8(&tmap2, w2->data, w2->k / 4, w2->n, 16 * prm.tgb, 2, who))) return st;
+    } else {
+        if ((st = cached_tmap_2d_u8(&tmap, w->data, w->k / 4, w->n, w->k / 4, 128, 16 * prm.tgb, true, who))) return st;
+        tmap2 = tmap;
+        if (dual &&
+            (st = cached_tmap_2d_u8(&tmap2, w2->data, w2->k / 4, w2->n, w2->k / 4, 128, 16 * prm.tgb, true, who)))
+            return st;
+    }
     {
         const HmLayout L(m, (int)w->k, (int)w->group, prm.tgb, prm.nstages, prm.tmax, dual ? 2 : 1);
         prm.ring = (uint32_t)L.ring;

@@ -178,7 +178,8 @@ def test_silu_mul_within_one_ulp(B):
 
 # ------------------------------------------------------------------------------ GEMV
 @pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 8])
-@pytest.mark.parametrize("n,k,group", [(37, 640, 128), (16, 128, 128), (300, 1024, 256), (1100, 2048, 128)])
+@pytest.mark.parametrize("n,k,group", [(37, 640, 128), (16, 128, 128), (300, 1024, 256), (1100, 2048, 128),
+                                       (48, 512, 128), (200, 1536, 256)])
 def test_gemv_small(B, m, n, k, group):
     d = synth.small_q2(400 + n + m, n, k, m, group=group)
     w = dev_q2(B, d["codes"], d["scales"], group)
