@@ -62,7 +62,8 @@ def test_dequant_full_prefill_weight(B):
 
 
 # ------------------------------------------------------------------------------ q8_1
-@pytest.mark.parametrize("m,k", [(1, 256), (3, 300), (5, 1000), (7, 5120), (2, 17408), (4, 8)])
+@pytest.mark.parametrize("m,k", [(1, 256), (3, 300), (5, 1000), (7, 5120), (2, 17408), (4, 8), (1030, 300),
+                                 (1100, 1000)])
 def test_q8_1_bitexact(B, m, k):
     x = synth.activations(synth._gen(300 + m + k), m, k, outlier_frac=0.3)
     out = u8_dev(B.quantize_act_q8_1(to_dev_u16_as_bf16(x)))
