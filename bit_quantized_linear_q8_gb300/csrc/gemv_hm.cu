@@ -40,6 +40,8 @@
 //    the running sums stay in registers over the whole K range.  At the end the P' partial
 //    sums of each row meet in shared memory and are added in a fixed order (results do not
 //    depend on timing), then stored as BF16 (with the FFN's SiLU*mul when asked).
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace bq8 {
@@ -264,7 +266,9 @@ __device__ __forceinline__ void consumer_sync() {
 
 // DUAL: one launch over the gate and up weights of an FFN (same shape), the warp's tile pair
 // being gate tile t and up tile t; the store forms u and h = SiLU(g) * u.
-template <int M, bool DUAL>
+// UNR: full chunks run a loop of constant trip count (two or four blocks a warp), a separate
+// instantiation so that the other launches keep their own register allocation.
+template <int M, bool DUAL, bool UNR>
 __global__ void __launch_bounds__(HM_THREADS, 1)
     q2_gemv_hm_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap2,
                       const HmParams p) {
@@ -534,7 +538,31 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
             const uint32_t cbase = ring32 + (uint32_t)ch.s * stage_bytes + (uint32_t)(tile0 - ch.gi * TGB) * HM_BOX + lane_c;
             const uint32_t sbase = srow32 + (uint32_t)(tile0 * 16 + g) * (uint32_t)G * 2u;
             const int pb0 = ch.kc * 8;
-            if (ntp == 2) {
+            // the warp's blocks of the chunk: blk = part + bi wpp.  In the UNR instantiation a full
+            // chunk (all 8 blocks inside the row) of two or four blocks a warp runs a loop of
+            // constant trip count that the compiler unrolls, so the next block's loads can be
+            // issued under the current block's MMAs; otherwise the counted loop.
+            auto blocks = [&](auto nt, auto nb) {
+                constexpr int NT = decltype(nt)::value, NB = decltype(nb)::value;
+#pragma unroll
+                for (int bi = 0; bi < NB; bi++) {
+                    const int blk = part + bi * wpp;
+                    const int pb = pb0 + blk;
+                    hm_block<NT, M>(tot, cbase + (uint32_t)(blk >> 2) * box_bytes + swz(blk), q1_off,
+                                    bbase + (uint32_t)pb * (256u * M), sbase + (uint32_t)(pb >> gsh) * 2u, q1_s2, G8);
+                }
+            };
+            using I1 = std::integral_constant<int, 1>;
+            using I2 = std::integral_constant<int, 2>;
+            using I4 = std::integral_constant<int, 4>;
+            const bool whole = UNR && pb0 + 8 <= P;
+            if (UNR && whole && nbw == 2) {
+                if (ntp == 2) blocks(I2{}, I2{});
+                else blocks(I1{}, I2{});
+            } else if (UNR && whole && nbw == 4) {
+                if (ntp == 2) blocks(I2{}, I4{});
+                else blocks(I1{}, I4{});
+            } else if (ntp == 2) {
                 for (int bi = 0; bi < nbw; bi++) {
                     const int blk = part + bi * wpp;  // pack block within the chunk, 0..7
                     const int pb = pb0 + blk;
@@ -663,17 +691,17 @@ bool gemv_hm_dual_supported(const bq_q2_weight* gate, uint32_t m) {
 
 typedef void (*HmKernel)(const CUtensorMap, const CUtensorMap, const HmParams);
 
-template <bool DUAL>
+template <bool DUAL, bool UNR>
 static HmKernel hm_kernel_for(uint32_t m) {
     switch (m) {
-        case 1: return q2_gemv_hm_kernel<1, DUAL>;
-        case 2: return q2_gemv_hm_kernel<2, DUAL>;
-        case 3: return q2_gemv_hm_kernel<3, DUAL>;
-        case 4: return q2_gemv_hm_kernel<4, DUAL>;
-        case 5: return q2_gemv_hm_kernel<5, DUAL>;
-        case 6: return q2_gemv_hm_kernel<6, DUAL>;
-        case 7: return q2_gemv_hm_kernel<7, DUAL>;
-        case 8: return q2_gemv_hm_kernel<8, DUAL>;
+        case 1: return q2_gemv_hm_kernel<1, DUAL, UNR>;
+        case 2: return q2_gemv_hm_kernel<2, DUAL, UNR>;
+        case 3: return q2_gemv_hm_kernel<3, DUAL, UNR>;
+        case 4: return q2_gemv_hm_kernel<4, DUAL, UNR>;
+        case 5: return q2_gemv_hm_kernel<5, DUAL, UNR>;
+        case 6: return q2_gemv_hm_kernel<6, DUAL, UNR>;
+        case 7: return q2_gemv_hm_kernel<7, DUAL, UNR>;
+        case 8: return q2_gemv_hm_kernel<8, DUAL, UNR>;
         default: return nullptr;
     }
 }
@@ -682,7 +710,7 @@ static HmKernel hm_kernel_for(uint32_t m) {
 // y2 gets u).
 static int launch_hm(const uint16_t* x, const bq_q2_weight* w, const bq_q2_weight* w2, uint16_t* y, uint16_t* y2,
                      uint32_t m, uint16_t* hgate, cudaStream_t stream, const char* who) {
-    static int configured_smem[64][2][8] = {};
+    static int configured_smem[64][3][8] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 64) dev = 63;
@@ -692,11 +720,15 @@ static int launch_hm(const uint16_t* x, const bq_q2_weight* w, const bq_q2_weigh
     size_t smem = 0;
     const int ncta = hm_plan((int)m, (int)w->n, (int)w->k, (int)w->group, dual ? 2 : 1, sm_count(), &prm, &smem);
     if (smem > (size_t)HM_SMEM_LIMIT) return fail(BQ_ERR_INVALID, "%s: shape needs too much shared memory", who);
-    const HmKernel kern = dual ? hm_kernel_for<true>(m) : hm_kernel_for<false>(m);
-    if ((size_t)configured_smem[dev][dual][m - 1] < smem) {
+    // single weight with two or four blocks a warp per chunk: the unrolled instantiation
+    const bool unr = !dual && hm_parts(prm.tgb, 1) <= 4;
+    const int kind = dual ? 1 : unr ? 2 : 0;
+    const HmKernel kern = dual ? hm_kernel_for<true, false>(m) : unr ? hm_kernel_for<false, true>(m)
+                                                                     : hm_kernel_for<false, false>(m);
+    if ((size_t)configured_smem[dev][kind][m - 1] < smem) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return fail(BQ_ERR_LAUNCH, "%s: cannot reserve %zu bytes of shared memory", who, smem);
-        configured_smem[dev][dual][m - 1] = (int)smem;
+        configured_smem[dev][kind][m - 1] = (int)smem;
     }
     // rows of a whole number of 128-byte column blocks (k % 512 == 0): one 3-D request brings a chunk's
     // two column blocks; otherwise two 2-D boxes per chunk
