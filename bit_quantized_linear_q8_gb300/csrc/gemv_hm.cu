@@ -542,11 +542,11 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
             // chunk (all 8 blocks inside the row) of two or four blocks a warp runs a loop of
             // constant trip count that the compiler unrolls, so the next block's loads can be
             // issued under the current block's MMAs; otherwise the counted loop.
-            auto blocks = [&](auto nt, auto nb) {
+            auto blocks = [&](auto nt, auto nb, int bi0) {
                 constexpr int NT = decltype(nt)::value, NB = decltype(nb)::value;
 #pragma unroll
                 for (int bi = 0; bi < NB; bi++) {
-                    const int blk = part + bi * wpp;
+                    const int blk = part + (bi0 + bi) * wpp;
                     const int pb = pb0 + blk;
                     hm_block<NT, M>(tot, cbase + (uint32_t)(blk >> 2) * box_bytes + swz(blk), q1_off,
                                     bbase + (uint32_t)pb * (256u * M), sbase + (uint32_t)(pb >> gsh) * 2u, q1_s2, G8);
@@ -557,11 +557,19 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
             using I4 = std::integral_constant<int, 4>;
             const bool whole = UNR && pb0 + 8 <= P;
             if (UNR && whole && nbw == 2) {
-                if (ntp == 2) blocks(I2{}, I2{});
-                else blocks(I1{}, I2{});
+                if (ntp == 2) blocks(I2{}, I2{}, 0);
+                else blocks(I1{}, I2{}, 0);
             } else if (UNR && whole && nbw == 4) {
-                if (ntp == 2) blocks(I2{}, I4{});
-                else blocks(I1{}, I4{});
+                // the dual form unrolls two blocks at a time: its second weight's state leaves no
+                // registers for four blocks in flight
+                if (DUAL) {
+                    blocks(I2{}, I2{}, 0);
+                    blocks(I2{}, I2{}, 2);
+                } else if (ntp == 2) {
+                    blocks(I2{}, I4{}, 0);
+                } else {
+                    blocks(I1{}, I4{}, 0);
+                }
             } else if (ntp == 2) {
                 for (int bi = 0; bi < nbw; bi++) {
                     const int blk = part + bi * wpp;  // pack block within the chunk, 0..7
@@ -710,7 +718,7 @@ static HmKernel hm_kernel_for(uint32_t m) {
 // y2 gets u).
 static int launch_hm(const uint16_t* x, const bq_q2_weight* w, const bq_q2_weight* w2, uint16_t* y, uint16_t* y2,
                      uint32_t m, uint16_t* hgate, cudaStream_t stream, const char* who) {
-    static int configured_smem[64][3][8] = {};
+    static int configured_smem[64][4][8] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 64) dev = 63;
@@ -720,11 +728,11 @@ static int launch_hm(const uint16_t* x, const bq_q2_weight* w, const bq_q2_weigh
     size_t smem = 0;
     const int ncta = hm_plan((int)m, (int)w->n, (int)w->k, (int)w->group, dual ? 2 : 1, sm_count(), &prm, &smem);
     if (smem > (size_t)HM_SMEM_LIMIT) return fail(BQ_ERR_INVALID, "%s: shape needs too much shared memory", who);
-    // single weight with two or four blocks a warp per chunk: the unrolled instantiation
-    const bool unr = !dual && hm_parts(prm.tgb, 1) <= 4;
-    const int kind = dual ? 1 : unr ? 2 : 0;
-    const HmKernel kern = dual ? hm_kernel_for<true, false>(m) : unr ? hm_kernel_for<false, true>(m)
-                                                                     : hm_kernel_for<false, false>(m);
+    // two or four blocks a warp per chunk: the unrolled instantiation
+    const bool unr = hm_parts(prm.tgb, dual ? 2 : 1) <= 4;  // two or four blocks a warp per chunk
+    const int kind = (dual ? 1 : 0) + (unr ? 2 : 0);
+    const HmKernel kern = dual ? (unr ? hm_kernel_for<true, true>(m) : hm_kernel_for<true, false>(m))
+                               : (unr ? hm_kernel_for<false, true>(m) : hm_kernel_for<false, false>(m));
     if ((size_t)configured_smem[dev][kind][m - 1] < smem) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return fail(BQ_ERR_LAUNCH, "%s: cannot reserve %zu bytes of shared memory", who, smem);
