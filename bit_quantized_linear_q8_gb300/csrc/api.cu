@@ -225,7 +225,7 @@ extern "C" {
 
 int bq_device_status(void) {
     const unsigned int s = bq8::gemv_status_take() | bq8::gemv_hm_status_take() | bq8::mmq_tc_status_take() |
-                           bq8::gemm_bf16_status_take();
+                           bq8::gemm_bf16_status_take() | bq8::q8_status_take();
     if (s) return bq8::fail(BQ_ERR_DEVICE, "a kernel gave up on a bounded wait (status bits 0x%x)", s);
     return bq8::ok();
 }

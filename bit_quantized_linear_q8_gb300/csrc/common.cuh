@@ -56,6 +56,7 @@ unsigned int gemv_status_take();
 unsigned int gemv_hm_status_take();
 unsigned int mmq_tc_status_take();
 unsigned int gemm_bf16_status_take();
+unsigned int q8_status_take();
 
 // The FP16 warp-MMA GEMV (gemv_hm.cu) and the shapes it takes.
 bool gemv_hm_supported(const bq_q2_weight* w, uint32_t m);

@@ -3,8 +3,8 @@
 //
 // All of these are streaming kernels without shared memory: coalesced 8/16-byte accesses,
 // grids sized as a multiple of the SM count (the NVFP4 dequant keeps the page's one CTA per
-// row).  The q8_1 quantiser is bound by instruction issue (one IEEE division per value for
-// the bit-exact rounding), the others by memory.
+// row), except the q8_1 quantiser for k % 256 == 0, which stages its input through shared
+// memory with bulk copies and replaces the IEEE division per value by an exact FMA form.
 #include "common.cuh"
 
 namespace bq8 {
@@ -78,7 +78,8 @@ __global__ void __launch_bounds__(256) q2_dequant_kernel(const uint8_t* __restri
 // =====================================================================================
 // q8_1 quantisation.  Thread -> 8 values; a quad of 4 threads owns one 32-value block.
 // d = amax/127, q = round-half-away(x/d), s = d*sum(q), every step an IEEE fp32
-// operation rounded to nearest (explicit _rn intrinsics, no contraction).
+// operation rounded to nearest (explicit _rn intrinsics, no contraction).  This form takes
+// any k (zero padding to kp); k % 256 == 0 goes to q8_1_block_kernel below.
 // Source: q4k_mmq.rs, `quantize_act_q8_1`.
 // =====================================================================================
 template <bool VEC>
@@ -130,6 +131,209 @@ __global__ void __launch_bounds__(256) q8_1_kernel(const uint16_t* __restrict__ 
         }
         *reinterpret_cast<uint2*>(codes + r * kp + c0) = make_uint2(lo, hi);
         if ((threadIdx.x & 3) == 0) ds[r * (kp / 32) + c0 / 32] = make_float2(d, __fmul_rn(d, (float)sum));
+    }
+}
+
+// -------------------------------------------------------------------------------------
+// q8_1 for k % 256 == 0 (then kp == k and the rows of x, of the codes and of the (d, s)
+// pairs are each one flat array): the flat value range is cut into units of Q8U values,
+// copied into shared memory by one bulk copy each (a ring of Q8S stages per CTA, refilled by
+// a producer warp), so that the bytes in flight do not depend on the consumers' registers.
+// Units are 16 KB because a bulk request costs the SM a roughly fixed time (4 KB ones held
+// the whole GPU near 2.7 TB/s).  One consumer thread takes one 32-value block: its amax
+// from BF16 pair maxima, its codes, the sum of its codes by dp4a, and its (d, s) pair.
+//
+// The codes are those of the IEEE sequence above, code = round-half-away(RN(x / d)) with
+// d = RN(amax / 127), computed without a division per value:
+//  * RN(a / d) for a = |x| is Markstein's correction of y0 = RN(a r) with r = RN(1/d):
+//    RN(y0 + r RN(a - d y0)), two FMAs (P. Markstein, "Computation of elementary functions on
+//    the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990: with a correctly
+//    rounded reciprocal and a quotient within an ulp, one correction rounds correctly).
+//  * round-half-away of that y >= 0 is floor(RZ(y + 1/2)) (the integers are representable,
+//    so rounding the sum toward zero never crosses one), and a second round-toward-zero add
+//    of 2^23 leaves it in the low mantissa byte.
+//  * d = RN(amax / 127) from q0 = RN(amax c), c = RN(1/127), and one FMA correction of the
+//    exact residual amax - 127 q0.
+// Both forms are checked on the host against the IEEE divisions for every BF16 pair
+// |x| <= amax of several binades (tests/test_q8_1_arith.py); the quotient can differ only
+// where the residual underflows, for quotients below 2^-100 whose code is 0.  Scaling by
+// powers of two keeps all of it exact while d is normal, so blocks with amax >= 2^-94 take
+// this path and smaller ones the IEEE divisions.  The four code bytes of a word are gathered
+// with byte permutes and the signs applied to all four at once.
+// -------------------------------------------------------------------------------------
+static __device__ unsigned int g_q8_status;
+
+unsigned int q8_status_take() {
+    unsigned int v = 0, zero = 0;
+    cudaMemcpyFromSymbol(&v, g_q8_status, sizeof v);
+    cudaMemcpyToSymbol(g_q8_status, &zero, sizeof zero);
+    return v;
+}
+
+constexpr int Q8U = 8192;                // values per unit (16 KB of BF16 in)
+constexpr int Q8S = 3;                   // ring stages per CTA
+constexpr int Q8C = Q8U / 32;           // consumer threads (one 32-value block each)
+constexpr int Q8T = Q8C + 32;            // plus one producer warp
+constexpr int Q8_CTAS_PER_SM = 4;
+constexpr int Q8_SMEM = Q8S * Q8U * 2 + 2 * Q8S * 8;
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Four codes with magnitudes c (0..127, the low byte of each of m0..m3) and the signs of the
+// BF16 values in bytes 1 and 3 of w0 and w1, as one word of int8 codes.  Each sign byte is
+// 0x00 or 0xFF (prmt's sign-replicating selector); -c per byte is ((c ^ 0xFF) & 0x7F) + 1
+// with the top bit flipped, which never carries into the next byte (c = 0 gives 0x80 ^ 0x80).
+__device__ __forceinline__ uint32_t q8_pack4(uint32_t m0, uint32_t m1, uint32_t m2, uint32_t m3, uint32_t w0,
+                                             uint32_t w1) {
+    const uint32_t mag = prmt(prmt(m0, m1, 0x0040u), prmt(m2, m3, 0x0040u), 0x5410u);
+    const uint32_t sgn = prmt(w0, w1, 0xFDB9u);
+    const uint32_t low = ((mag ^ sgn) & 0x7F7F7F7Fu) + (sgn & 0x01010101u);
+    return low ^ (sgn & 0x80808080u);
+}
+
+// 2^23 + |code| as float bits, by IEEE division (any d > 0): floor(RZ(|y| + 1/2)) equals
+// floor(|y| + 1/2) because the integers are representable; clamped to 127.
+__device__ __forceinline__ uint32_t q8_mag_div(float v, float d) {
+    const float a = fminf(__fadd_rz(fabsf(__fdiv_rn(v, d)), 0.5f), 127.0f);
+    return __float_as_uint(__fadd_rz(a, 8388608.0f));
+}
+
+// The same bits without a division per value (d normal, r = RN(1/d)).
+__device__ __forceinline__ uint32_t q8_mag_fast(float v, float d, float r) {
+    const float a = fabsf(v);
+    const float y0 = __fmul_rn(a, r);
+    const float y = __fmaf_rn(__fmaf_rn(-d, y0, a), r, y0);  // RN(a / d)
+    return __float_as_uint(__fadd_rz(__fadd_rz(y, 0.5f), 8388608.0f));
+}
+
+// RN(amax / 127) for a BF16 amax >= 2^-94.
+__device__ __forceinline__ float q8_scale(float amax) {
+    constexpr float c127 = 1.0f / 127.0f;
+    const float q0 = __fmul_rn(amax, c127);
+    return __fmaf_rn(__fmaf_rn(-q0, 127.0f, amax), c127, q0);
+}
+
+// Producer warp of the flat q8_1 kernels: one bulk copy per unit into the ring.
+__device__ __forceinline__ void q8_produce(const uint16_t* __restrict__ x, uint8_t (*stage)[Q8U * 2], uint64_t* full,
+                                           uint64_t* empty, int64_t total) {
+    const int64_t units = (total + Q8U - 1) / Q8U;
+    int64_t i = 0;
+    bool ok = true;
+    for (int64_t u = blockIdx.x; u < units; u += gridDim.x, i++) {
+        const int s = (int)(i % Q8S);
+        if (i >= Q8S && !mbar_wait_suspend(&empty[s], (uint32_t)((i / Q8S - 1) & 1))) {
+            ok = false;
+            break;
+        }
+        const int64_t len = min((int64_t)Q8U, total - u * Q8U);
+        mbar_arrive_expect_tx(&full[s], (uint32_t)(len * 2));
+        bulk_load(stage[s], x + u * Q8U, (uint32_t)(len * 2), &full[s]);
+    }
+    // every copy issued has landed before the CTA ends (the consumers waited for all of them
+    // unless one gave up)
+    for (int64_t j = (i > Q8S ? i - Q8S : 0); j < i; j++)
+        if (!mbar_wait_suspend(&full[j % Q8S], (uint32_t)((j / Q8S) & 1))) ok = false;
+    if (!ok) atomicOr(&g_q8_status, 1u);
+}
+
+// One consumer thread per 32-value block: the block's four 16-byte chunks are read in an
+// order rotated by (thread / 2) % 4, which puts the eight threads of each shared-memory
+// phase on distinct banks, and its codes are stored in that order.
+__global__ void __launch_bounds__(Q8T, Q8_CTAS_PER_SM)
+    q8_1_block_kernel(const uint16_t* __restrict__ x, int8_t* __restrict__ codes, float2* __restrict__ ds,
+                      int64_t total) {
+    extern __shared__ __align__(128) uint8_t q8_smem[];
+    uint8_t(*stage)[Q8U * 2] = reinterpret_cast<uint8_t(*)[Q8U * 2]>(q8_smem);
+    uint64_t* full = reinterpret_cast<uint64_t*>(q8_smem + Q8S * Q8U * 2);
+    uint64_t* empty = full + Q8S;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t units = (total + Q8U - 1) / Q8U;
+    if (tid < Q8S) {
+        mbar_init(&full[tid], 1);
+        mbar_init(&empty[tid], Q8C / 32);
+    }
+    fence_barrier_init();
+    __syncthreads();
+    if (warp == Q8C / 32) {
+        if (lane == 0) q8_produce(x, stage, full, empty, total);
+        return;
+    }
+    const int rot = (tid >> 1) & 3;
+    int64_t i = 0;
+    for (int64_t u = blockIdx.x; u < units; u += gridDim.x, i++) {
+        const int s = (int)(i % Q8S);
+        const bool ok = mbar_wait_suspend(&full[s], (uint32_t)((i / Q8S) & 1));
+        if (__any_sync(0xffffffffu, !ok)) {
+            if (lane == 0) atomicOr(&g_q8_status, 2u);
+            break;
+        }
+        const int64_t len = min((int64_t)Q8U, total - u * Q8U);  // a multiple of 256
+        if (32 * tid < len) {
+            uint4 c[4];
+#pragma unroll
+            for (int j = 0; j < 4; j++)
+                c[j] = *reinterpret_cast<const uint4*>(stage[s] + 64 * tid + 16 * ((j + rot) & 3));
+            __nv_bfloat162 m2 = bits_bf162(c[0].x & 0x7FFF7FFFu);
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                if (j) m2 = __hmax2(m2, bits_bf162(c[j].x & 0x7FFF7FFFu));
+                m2 = __hmax2(m2, bits_bf162(c[j].y & 0x7FFF7FFFu));
+                m2 = __hmax2(m2, bits_bf162(c[j].z & 0x7FFF7FFFu));
+                m2 = __hmax2(m2, bits_bf162(c[j].w & 0x7FFF7FFFu));
+            }
+            const uint32_t mb = bf162_bits(m2);
+            const float amax = fmaxf(__uint_as_float(mb << 16), __uint_as_float(mb & 0xFFFF0000u));
+            float d;
+            uint32_t pk[8];
+#pragma unroll
+            for (int j = 0; j < 8; j++) pk[j] = 0;
+            if (amax >= 0x1p-94f) {
+                d = q8_scale(amax);
+                const float r = __frcp_rn(d);
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const uint4 w = c[j];
+                    pk[2 * j] = q8_pack4(q8_mag_fast(__uint_as_float(w.x << 16), d, r),
+                                         q8_mag_fast(__uint_as_float(w.x & 0xFFFF0000u), d, r),
+                                         q8_mag_fast(__uint_as_float(w.y << 16), d, r),
+                                         q8_mag_fast(__uint_as_float(w.y & 0xFFFF0000u), d, r), w.x, w.y);
+                    pk[2 * j + 1] = q8_pack4(q8_mag_fast(__uint_as_float(w.z << 16), d, r),
+                                             q8_mag_fast(__uint_as_float(w.z & 0xFFFF0000u), d, r),
+                                             q8_mag_fast(__uint_as_float(w.w << 16), d, r),
+                                             q8_mag_fast(__uint_as_float(w.w & 0xFFFF0000u), d, r), w.z, w.w);
+                }
+            } else {
+                d = __fdiv_rn(amax, 127.0f);
+                if (amax != 0.0f) {
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        const uint4 w = c[j];
+                        pk[2 * j] = q8_pack4(q8_mag_div(__uint_as_float(w.x << 16), d),
+                                             q8_mag_div(__uint_as_float(w.x & 0xFFFF0000u), d),
+                                             q8_mag_div(__uint_as_float(w.y << 16), d),
+                                             q8_mag_div(__uint_as_float(w.y & 0xFFFF0000u), d), w.x, w.y);
+                        pk[2 * j + 1] = q8_pack4(q8_mag_div(__uint_as_float(w.z << 16), d),
+                                                 q8_mag_div(__uint_as_float(w.z & 0xFFFF0000u), d),
+                                                 q8_mag_div(__uint_as_float(w.w << 16), d),
+                                                 q8_mag_div(__uint_as_float(w.w & 0xFFFF0000u), d), w.z, w.w);
+                    }
+                }
+            }
+            int sum = 0;
+#pragma unroll
+            for (int j = 0; j < 8; j++) sum = __dp4a((int)pk[j], 0x01010101, sum);
+            int8_t* dst = codes + u * Q8U + 32 * tid;
+#pragma unroll
+            for (int j = 0; j < 4; j++)
+                *reinterpret_cast<uint2*>(dst + 8 * ((j + rot) & 3)) = make_uint2(pk[2 * j], pk[2 * j + 1]);
+            ds[u * (Q8U / 32) + tid] = make_float2(d, __fmul_rn(d, (float)sum));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
     }
 }
 
@@ -398,6 +602,24 @@ int quantize_act_q8_1(const uint16_t* x, void* act_q8, uint32_t m, uint32_t k, b
     const int64_t kp = ((int64_t)k + 255) / 256 * 256;
     int8_t* codes = (int8_t*)act_q8;
     float2* ds = (float2*)((uint8_t*)act_q8 + (int64_t)m * kp);
+    if (k % 256 == 0) {
+        const int64_t total = (int64_t)m * k;
+        const int64_t units = (total + Q8U - 1) / Q8U;
+        const int64_t cap = (int64_t)sm_count() * Q8_CTAS_PER_SM;
+        static int configured[64] = {};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+            return fail(BQ_ERR_LAUNCH, "quantize_act_q8_1: no current CUDA device");
+        if (!configured[dev]) {
+            if (cudaFuncSetAttribute(q8_1_block_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Q8_SMEM) !=
+                cudaSuccess)
+                return fail(BQ_ERR_LAUNCH, "quantize_act_q8_1: cannot reserve %d bytes of shared memory", Q8_SMEM);
+            configured[dev] = 1;
+        }
+        q8_1_block_kernel<<<(unsigned)(units < cap ? units : cap), Q8T, Q8_SMEM, (cudaStream_t)stream>>>(x, codes, ds,
+                                                                                                     total);
+        return check_launch("quantize_act_q8_1");
+    }
     const int64_t work = (int64_t)m * kp / 8;
     if (k % 8 == 0)
         q8_1_kernel<true><<<grid_for(work, 256), 256, 0, (cudaStream_t)stream>>>(x, codes, ds, m, k, kp);

@@ -27,7 +27,9 @@
 //    columns, one TMA box of 128 bytes x 16 tiles-per-group rows per 512-column half, with
 //    the 128-byte swizzle so that the eight rows a warp reads at once fall on distinct banks.
 //    The boxes are tall on purpose: a TMA request costs an SM a roughly fixed time, so boxes
-//    of 2 KB stream at a fifth of the rate of 16 KB ones.  A producer warp requests the
+//    of 2 KB stream at a fifth of the rate of 16 KB ones.  Where K is a multiple of 512 the
+//    weight is also described as a 3-D tensor (128-byte column block, row, block) so that
+//    one request brings both halves of a chunk.  A producer warp requests the
 //    chunks into a ring (mbarrier "full" per stage, transaction bytes) and refills a stage
 //    once every consumer warp has arrived on its "empty" barrier; the ring usually holds the
 //    CTA's whole slice.  The first chunk and the CTA's scales (one bulk copy) are requested at
@@ -37,7 +39,11 @@
 //  * Compute: sixteen consumer warps.  Warp w takes the tile pair w / P' of every row group
 //    (two independent MMA chains) and pack blocks w % P', w % P' + P', ... of every chunk
 //    (P' warps share a pair), so the B fragments of a block are loaded once for two tiles and
-//    the running sums stay in registers over the whole K range.  At the end the P' partial
+//    the running sums stay in registers over the whole K range.  When a warp takes two or four
+//    blocks of a full chunk, a second instantiation runs them as an unrolled loop, so that the
+//    next block's shared-memory loads issue under the current block's MMAs.  The launch
+//    constants (shared-memory layout, the reciprocals that replace divisions) are computed
+//    on the host.  At the end the P' partial
 //    sums of each row meet in shared memory and are added in a fixed order (results do not
 //    depend on timing), then stored as BF16 (with the FFN's SiLU*mul when asked).
 #include <type_traits>

@@ -111,6 +111,29 @@ def test_q8_1_half_integer_boundaries(B):
     assert np.array_equal(out, O.quantize_q8_1(xb))
 
 
+def test_q8_1_block_scale_range(B):
+    """Blocks whose maxima span the whole BF16 range, subnormals included (the quantiser takes
+    d = RN(amax / 127) without a division for amax >= 2^-94 and by IEEE division below), with
+    values on and beside the half-integer points of x / d, and a row of maxima only."""
+    import torch
+    rng = np.random.default_rng(94)
+    m, k = 192, 512
+    e = rng.integers(-133, 127, size=(m, k // 32))
+    e[:8] = np.arange(-98, -90).reshape(8, 1)   # around the switch between the two forms
+    amax = np.ldexp(rng.uniform(1.0, 2.0, size=(m, k // 32)), e).astype(np.float32)
+    amax_b = torch.tensor(amax).to(torch.bfloat16).to(torch.float32).numpy()
+    h = rng.integers(0, 127, size=(m, k)) + rng.choice([0.0, 0.5], size=(m, k))
+    x = (h * np.repeat(amax_b, 32, axis=1) / 127.0) * rng.choice([-1.0, 1.0], size=(m, k))
+    xb = torch.tensor(x.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+    step = rng.integers(-1, 2, size=(m, k)).astype(np.int32)
+    xb = np.where(xb & 0x7FFF, (xb.astype(np.int32) + step) & 0xFFFF, xb).astype(np.uint16)
+    ab = torch.tensor(amax_b).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    xb[:, ::32] = ab                            # each block holds its maximum
+    xb[-1] = np.repeat(ab[-1], 32)              # a row of maxima only
+    out = u8_dev(B.quantize_act_q8_1(to_dev_u16_as_bf16(xb)))
+    assert np.array_equal(out, O.quantize_q8_1(xb))
+
+
 # ------------------------------------------------------------------------------ NVFP4 -> BF16
 def _nvfp4(B, d, scale2=None):
     import torch
