@@ -24,12 +24,13 @@
 //  * Work split: the n rows form 16-row tiles; CTA c takes tiles [c T / C, (c + 1) T / C), a
 //    contiguous byte range of the weight, so every SM streams the same bytes to within a tile.
 //  * Staging: the CTA's tiles form row groups of up to eight; a chunk is one row group x 1024
-//    columns, one TMA box of 128 bytes x 16 tiles-per-group rows per 512-column half, with
+//    columns (2048 for few long rows per CTA, see hm_plan), one TMA box of 128 bytes x 16
+//    tiles-per-group rows per 512-column half, with
 //    the 128-byte swizzle so that the eight rows a warp reads at once fall on distinct banks.
 //    The boxes are tall on purpose: a TMA request costs an SM a roughly fixed time, so boxes
 //    of 2 KB stream at a fifth of the rate of 16 KB ones.  Where K is a multiple of 512 the
 //    weight is also described as a 3-D tensor (128-byte column block, row, block) so that
-//    one request brings both halves of a chunk.  A producer warp requests the
+//    one request brings all halves of a chunk.  A producer warp requests the
 //    chunks into a ring (mbarrier "full" per stage, transaction bytes) and refills a stage
 //    once every consumer warp has arrived on its "empty" barrier; the ring usually holds the
 //    CTA's whole slice.  The first chunk and the CTA's scales (one bulk copy) are requested at
@@ -96,6 +97,7 @@ struct HmParams {
     uint32_t cmag;           // ceil(2^32 / CTAs): the CTA's tile range by a multiply-high
     uint32_t gmag;           // ceil(2^32 / tgb): the CTA's row groups by a multiply-high
     int chunk3d;             // 1: the maps are 3-D chunk maps, one request per weight and chunk
+    int hpc;                 // 512-column halves per chunk (the kernel's HPC; host side)
 };
 
 // x / d by a multiply-high with mag = ceil(2^32 / d) computed in 32 bits, which wraps to 0
@@ -113,10 +115,10 @@ __host__ __device__ inline int hm_parts(int tgb, int nw) {
 // nw = 2 for the dual (gate and up) form.
 struct HmLayout {
     size_t ring, btab, scal, scal_w, slot, misc, total;
-    __host__ __device__ HmLayout(int m, int k, int group, int tgb, int nstages, int tmax, int nw) {
+    __host__ __device__ HmLayout(int m, int k, int group, int tgb, int nstages, int tmax, int nw, int hpc) {
         const size_t P = (size_t)k / 128, G = (size_t)k / group;
-        ring = 0;                                                       // [stage][nw][2 halves][16 tgb rows][128 B]
-        btab = ring + (size_t)nstages * nw * 2 * tgb * HM_BOX;          // [P][4 quads][m][4 lanes][16 B]
+        ring = 0;                                                       // [stage][nw][hpc halves][16 tgb rows][128 B]
+        btab = ring + (size_t)nstages * nw * hpc * tgb * HM_BOX;        // [P][4 quads][m][4 lanes][16 B]
         scal = btab + P * (size_t)m * 256;                              // [nw] CTA's scale rows (+ alignment)
         scal_w = ((size_t)tmax * 16 * G * 2 + 32 + 15) & ~size_t(15);
         slot = scal + nw * scal_w;                                      // [parts][nw][16 tmax rows][m] fp32
@@ -211,7 +213,7 @@ __device__ __forceinline__ void hm_tiles(float (&ac)[HM_TG][4], const uint2 (&w)
 #undef HM_POS
 }
 
-// Where a chunk sits: its stage and the stage's phase parity, its row group and 1024-column
+// Where a chunk sits: its stage and the stage's phase parity, its row group and column
 // step.  Advanced by counting (no division in the loop).
 struct HmCursor {
     int s, gi, kc;
@@ -274,7 +276,8 @@ __device__ __forceinline__ void consumer_sync() {
 // being gate tile t and up tile t; the store forms u and h = SiLU(g) * u.
 // UNR: full chunks run a loop of constant trip count (two or four blocks a warp), a separate
 // instantiation so that the other launches keep their own register allocation.
-template <int M, bool DUAL, bool UNR>
+// HPC: 512-column halves per chunk, 2 (1024 columns) or 4 (2048 columns).
+template <int M, bool DUAL, bool UNR, int HPC>
 __global__ void __launch_bounds__(HM_THREADS, 1)
     q2_gemv_hm_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap2,
                       const HmParams p) {
@@ -306,10 +309,11 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
     const int kb = k >> 2;  // code bytes per row
     const int NST = p.nstages, TGB = p.tgb;
     const int ngrp = (int)hm_div((uint32_t)(TC + TGB - 1), p.gmag);  // row groups
-    const int nkc = (P + 7) >> 3;               // 1024-column chunks per row group
+    constexpr int cbs = HPC == 4 ? 4 : 3;           // log2 pack blocks per chunk
+    const int nkc = (P + (1 << cbs) - 1) >> cbs;    // chunks per row group
     const int nch = ngrp * nkc;
     const uint32_t box_bytes = (uint32_t)TGB * HM_BOX;
-    const uint32_t stage_bytes = NW * 2 * box_bytes;  // [weight][half][box]
+    const uint32_t stage_bytes = NW * HPC * box_bytes;  // [weight][half][box]
 
     // the CTA's scales: bytes [s_lo, s_hi) of the plane by one bulk copy, the rest (at most
     // 14 bytes at the end of the plane) by plain loads
@@ -367,20 +371,22 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
                 }
                 uint8_t* dst = ring + (size_t)cur.s * stage_bytes;
                 if (p.chunk3d) {
-                    // one request per weight: both 512-column halves (128-byte column blocks 2 kc
-                    // and 2 kc + 1) of 16 TGB rows, the layout of the two 2-D boxes below
-                    mbar_arrive_expect_tx(&full[cur.s], (uint32_t)(NW * 2) * box_bytes);
+                    // one request per weight: the chunk's HPC 512-column halves (128-byte column
+                    // blocks HPC kc ..) of 16 TGB rows, the layout of the 2-D boxes below (blocks
+                    // past the row's end arrive as zeros and are never read)
+                    mbar_arrive_expect_tx(&full[cur.s], (uint32_t)(NW * HPC) * box_bytes);
                     for (int w = 0; w < NW; w++)
-                        tma_load_3d(dst + (size_t)(w * 2) * box_bytes, w ? &tmap2 : &tmap, 0, r0 + 16 * cur.gi * TGB,
-                                    2 * cur.kc, &full[cur.s]);
+                        tma_load_3d(dst + (size_t)(w * HPC) * box_bytes, w ? &tmap2 : &tmap, 0,
+                                    r0 + 16 * cur.gi * TGB, HPC * cur.kc, &full[cur.s]);
                 } else {
                     // one box of 128 bytes x 16 TGB rows per 512-column half that starts inside the row
-                    const int nh = cur.kc * 256 + 128 < kb ? 2 : 1;
+                    int nh = 0;
+                    while (nh < HPC && (cur.kc * HPC + nh) * 128 < kb) nh++;
                     mbar_arrive_expect_tx(&full[cur.s], (uint32_t)(NW * nh) * box_bytes);
                     for (int w = 0; w < NW; w++)
                         for (int h = 0; h < nh; h++)
-                            tma_load_2d(dst + (size_t)(w * 2 + h) * box_bytes, w ? &tmap2 : &tmap,
-                                        cur.kc * 256 + h * 128, r0 + 16 * cur.gi * TGB, &full[cur.s]);
+                            tma_load_2d(dst + (size_t)(w * HPC + h) * box_bytes, w ? &tmap2 : &tmap,
+                                        (cur.kc * HPC + h) * 128, r0 + 16 * cur.gi * TGB, &full[cur.s]);
                 }
                 nis++;
                 if (c == (NST - 1 > HM_EARLY_CHUNKS ? NST - 1 : HM_EARLY_CHUNKS) && nch > NST) {
@@ -417,7 +423,10 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
     // from registers when every vector fitted in one load batch, else reloading.  A vector's
     // row v / kv is a multiply-high by ceil(2^32 / kv): exact while v (ceil(2^32 / kv) kv -
     // 2^32) < 2^32, i.e. for every v < 8 kv when kv < 23170 (the host keeps k below that).
-    constexpr int XV = 8;  // vectors of 8 values per thread and batch
+    // vectors of 8 values per thread and batch; the long-row (HPC = 4) form holds 2 * 17408
+    // values in one batch at M = 2, so that they are loaded once (at M = 3 a batch of 13
+    // vectors measured slower than two batches of 8)
+    constexpr int XV = HPC == 4 && M == 2 ? 9 : 8;
     constexpr int NCT = HM_CWARPS * 32;
     const int kv = k >> 3;     // 8-value vectors per row
     const int tv = M * kv;     // vectors of x
@@ -514,11 +523,11 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
     const int tlast = TC - (ngrp - 1) * TGB;  // tiles of the last row group
     const int wpp = 1 << p.lw;  // warps per tile pair (a power of two, at most 8)
     const int pair = warp >> p.lw, part = warp & (wpp - 1);
-    const int nbw = 8 >> p.lw;  // pack blocks per chunk and warp
+    const int nbw = (1 << cbs) >> p.lw;  // pack blocks per chunk and warp
     const int jb = min(g, M - 1);  // activation row of the lane's B fragments (columns >= M are never stored)
     const size_t pstride = (size_t)16 * p.tmax * M;  // one part's (and weight's) partial sums
     // second tile of a pair: the next tile of the box, or the same tile of the up weight
-    const uint32_t q1_off = DUAL ? 2 * box_bytes : HM_BOX;
+    const uint32_t q1_off = DUAL ? HPC * box_bytes : HM_BOX;
     const uint32_t ring32 = smem_u32(ring), srow32 = smem_u32(srow);
     const uint32_t lane_c = (uint32_t)(g * 128 + ((t & 1) << 3));               // row g, 8-byte half of a chunk
     const uint32_t bbase = smem_u32(btab) + (uint32_t)(jb * 4 + t) * 16u;       // + pb * 256 m
@@ -543,9 +552,9 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
             // fragments (block pb at pb * 256 m bytes) and its scales (block pb at (pb >> gsh) * 2)
             const uint32_t cbase = ring32 + (uint32_t)ch.s * stage_bytes + (uint32_t)(tile0 - ch.gi * TGB) * HM_BOX + lane_c;
             const uint32_t sbase = srow32 + (uint32_t)(tile0 * 16 + g) * (uint32_t)G * 2u;
-            const int pb0 = ch.kc * 8;
+            const int pb0 = ch.kc << cbs;
             // the warp's blocks of the chunk: blk = part + bi wpp.  In the UNR instantiation a full
-            // chunk (all 8 blocks inside the row) of two or four blocks a warp runs a loop of
+            // chunk (all its blocks inside the row) of two or four blocks a warp runs a loop of
             // constant trip count that the compiler unrolls, so the next block's loads can be
             // issued under the current block's MMAs; otherwise the counted loop.
             auto blocks = [&](auto nt, auto nb, int bi0) {
@@ -561,7 +570,7 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
             using I1 = std::integral_constant<int, 1>;
             using I2 = std::integral_constant<int, 2>;
             using I4 = std::integral_constant<int, 4>;
-            const bool whole = UNR && pb0 + 8 <= P;
+            const bool whole = UNR && pb0 + (1 << cbs) <= P;
             if (UNR && whole && nbw == 2) {
                 if (ntp == 2) blocks(I2{}, I2{}, 0);
                 else blocks(I1{}, I2{}, 0);
@@ -578,7 +587,7 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
                 }
             } else if (ntp == 2) {
                 for (int bi = 0; bi < nbw; bi++) {
-                    const int blk = part + bi * wpp;  // pack block within the chunk, 0..7
+                    const int blk = part + bi * wpp;  // pack block within the chunk
                     const int pb = pb0 + blk;
                     if (pb >= P) break;
                     hm_block<2, M>(tot, cbase + (uint32_t)(blk >> 2) * box_bytes + swz(blk), q1_off,
@@ -657,29 +666,38 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
 // tiles as balance the CTA's tiles over the fewest groups of at most eight (TMA requests
 // stream faster the larger they are: a box of 8 tiles is 16 KB); the ring gets as many
 // stages as one SM holds, up to one per chunk, so a CTA's whole slice is usually requested
-// at once.  nw = 2: the dual (gate and up) form.
+// at once.  A chunk spans 1024 columns, or 2048 where each tile pair of a single weight has
+// eight warps (one or two pairs per row group, as in an FFN's down projection: few rows, long
+// rows) and three such stages fit: each warp then takes two pack blocks per chunk, which halves the
+// per-chunk waits, releases and requests and lets the unrolled block loop run.  nw = 2: the
+// dual (gate and up) form.
 static int hm_plan(int m, int n, int k, int group, int nw, int sms, HmParams* prm, size_t* smem_out) {
     const int ntiles = (n + 15) / 16;
     const int ncta = ntiles < sms ? ntiles : sms;
     const int tmax = (ntiles + ncta - 1) / ncta;
-    const int nkc = (k / 128 + 7) / 8;
     // the fewest row groups whose two-stage ring fits, then as many stages as fit
     int ngrp = (tmax + HM_MAX_TGB - 1) / HM_MAX_TGB, tgb = (tmax + ngrp - 1) / ngrp;
-    while (tgb > 1 && HmLayout(m, k, group, tgb, 2, tmax, nw).total > (size_t)HM_SMEM_LIMIT) {
+    while (tgb > 1 && HmLayout(m, k, group, tgb, 2, tmax, nw, 2).total > (size_t)HM_SMEM_LIMIT) {
         ngrp++;
         tgb = (tmax + ngrp - 1) / ngrp;
     }
+    const int hpc = nw == 1 && hm_parts(tgb, nw) == HM_MAX_PARTS && k / 128 >= 16 &&
+                            HmLayout(m, k, group, tgb, 3, tmax, nw, 4).total <= (size_t)HM_SMEM_LIMIT
+                        ? 4
+                        : 2;
+    const int nkc = (k / 128 + 4 * hpc - 1) / (4 * hpc);
     const int nch = ngrp * nkc;
     int NST = HM_MAX_STAGES < nch ? HM_MAX_STAGES : nch;
     if (NST < 2) NST = 2;
-    while (NST > 2 && HmLayout(m, k, group, tgb, NST, tmax, nw).total > (size_t)HM_SMEM_LIMIT) NST--;
+    while (NST > 2 && HmLayout(m, k, group, tgb, NST, tmax, nw, hpc).total > (size_t)HM_SMEM_LIMIT) NST--;
     prm->n = n;
     prm->k = k;
     prm->group = group;
     prm->tmax = tmax;
     prm->tgb = tgb;
     prm->nstages = NST;
-    *smem_out = HmLayout(m, k, group, tgb, NST, tmax, nw).total;
+    prm->hpc = hpc;
+    *smem_out = HmLayout(m, k, group, tgb, NST, tmax, nw, hpc).total;
     return ncta;
 }
 
@@ -705,17 +723,17 @@ bool gemv_hm_dual_supported(const bq_q2_weight* gate, uint32_t m) {
 
 typedef void (*HmKernel)(const CUtensorMap, const CUtensorMap, const HmParams);
 
-template <bool DUAL, bool UNR>
+template <bool DUAL, bool UNR, int HPC>
 static HmKernel hm_kernel_for(uint32_t m) {
     switch (m) {
-        case 1: return q2_gemv_hm_kernel<1, DUAL, UNR>;
-        case 2: return q2_gemv_hm_kernel<2, DUAL, UNR>;
-        case 3: return q2_gemv_hm_kernel<3, DUAL, UNR>;
-        case 4: return q2_gemv_hm_kernel<4, DUAL, UNR>;
-        case 5: return q2_gemv_hm_kernel<5, DUAL, UNR>;
-        case 6: return q2_gemv_hm_kernel<6, DUAL, UNR>;
-        case 7: return q2_gemv_hm_kernel<7, DUAL, UNR>;
-        case 8: return q2_gemv_hm_kernel<8, DUAL, UNR>;
+        case 1: return q2_gemv_hm_kernel<1, DUAL, UNR, HPC>;
+        case 2: return q2_gemv_hm_kernel<2, DUAL, UNR, HPC>;
+        case 3: return q2_gemv_hm_kernel<3, DUAL, UNR, HPC>;
+        case 4: return q2_gemv_hm_kernel<4, DUAL, UNR, HPC>;
+        case 5: return q2_gemv_hm_kernel<5, DUAL, UNR, HPC>;
+        case 6: return q2_gemv_hm_kernel<6, DUAL, UNR, HPC>;
+        case 7: return q2_gemv_hm_kernel<7, DUAL, UNR, HPC>;
+        case 8: return q2_gemv_hm_kernel<8, DUAL, UNR, HPC>;
         default: return nullptr;
     }
 }
@@ -724,7 +742,7 @@ static HmKernel hm_kernel_for(uint32_t m) {
 // y2 gets u).
 static int launch_hm(const uint16_t* x, const bq_q2_weight* w, const bq_q2_weight* w2, uint16_t* y, uint16_t* y2,
                      uint32_t m, uint16_t* hgate, cudaStream_t stream, const char* who) {
-    static int configured_smem[64][4][8] = {};
+    static int configured_smem[64][5][8] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 64) dev = 63;
@@ -735,24 +753,29 @@ static int launch_hm(const uint16_t* x, const bq_q2_weight* w, const bq_q2_weigh
     const int ncta = hm_plan((int)m, (int)w->n, (int)w->k, (int)w->group, dual ? 2 : 1, sm_count(), &prm, &smem);
     if (smem > (size_t)HM_SMEM_LIMIT) return fail(BQ_ERR_INVALID, "%s: shape needs too much shared memory", who);
     // two or four blocks a warp per chunk: the unrolled instantiation
-    const bool unr = hm_parts(prm.tgb, dual ? 2 : 1) <= 4;  // two or four blocks a warp per chunk
-    const int kind = (dual ? 1 : 0) + (unr ? 2 : 0);
-    const HmKernel kern = dual ? (unr ? hm_kernel_for<true, true>(m) : hm_kernel_for<true, false>(m))
-                               : (unr ? hm_kernel_for<false, true>(m) : hm_kernel_for<false, false>(m));
+    const int nbw = 4 * prm.hpc / hm_parts(prm.tgb, dual ? 2 : 1);
+    const bool unr = nbw == 2 || nbw == 4;
+    // (hm_plan gives 2048-column chunks only to the single-weight form with eight warps per
+    // tile pair, i.e. always with two blocks a warp: the one HPC = 4 instantiation)
+    const int kind = prm.hpc == 4 ? 4 : (dual ? 1 : 0) + (unr ? 2 : 0);
+    const HmKernel kern = prm.hpc == 4 ? hm_kernel_for<false, true, 4>(m)
+                          : dual ? (unr ? hm_kernel_for<true, true, 2>(m) : hm_kernel_for<true, false, 2>(m))
+                                 : (unr ? hm_kernel_for<false, true, 2>(m) : hm_kernel_for<false, false, 2>(m));
     if ((size_t)configured_smem[dev][kind][m - 1] < smem) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return fail(BQ_ERR_LAUNCH, "%s: cannot reserve %zu bytes of shared memory", who, smem);
         configured_smem[dev][kind][m - 1] = (int)smem;
     }
     // rows of a whole number of 128-byte column blocks (k % 512 == 0): one 3-D request brings a chunk's
-    // two column blocks; otherwise two 2-D boxes per chunk
+    // column blocks; otherwise one 2-D box per 512-column half
     CUtensorMap tmap, tmap2;
     int st;
     prm.chunk3d = (w->k % 512 == 0) ? 1 : 0;
     if (prm.chunk3d) {
-        if ((st = cached_tmap_chunks_u8(&tmap, w->data, w->k / 4, w->n, 16 * prm.tgb, 2, who))) return st;
+        if ((st = cached_tmap_chunks_u8(&tmap, w->data, w->k / 4, w->n, 16 * prm.tgb, prm.hpc, who))) return st;
         tmap2 = tmap;
-        if (dual && (st = cached_tmap_chunks_u8(&tmap2, w2->data, w2->k / 4, w2->n, 16 * prm.tgb, 2, who))) return st;
+        if (dual && (st = cached_tmap_chunks_u8(&tmap2, w2->data, w2->k / 4, w2->n, 16 * prm.tgb, prm.hpc, who)))
+            return st;
     } else {
         if ((st = cached_tmap_2d_u8(&tmap, w->data, w->k / 4, w->n, w->k / 4, 128, 16 * prm.tgb, true, who))) return st;
         tmap2 = tmap;
@@ -761,7 +784,7 @@ static int launch_hm(const uint16_t* x, const bq_q2_weight* w, const bq_q2_weigh
             return st;
     }
     {
-        const HmLayout L(m, (int)w->k, (int)w->group, prm.tgb, prm.nstages, prm.tmax, dual ? 2 : 1);
+        const HmLayout L(m, (int)w->k, (int)w->group, prm.tgb, prm.nstages, prm.tmax, dual ? 2 : 1, prm.hpc);
         prm.ring = (uint32_t)L.ring;
         prm.btab = (uint32_t)L.btab;
         prm.scal = (uint32_t)L.scal;
