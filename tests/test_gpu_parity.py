@@ -212,9 +212,10 @@ def test_gemv_small(B, m, n, k, group):
     check_bf16_vs_f64(y, ref, "gemv m=%d n=%d k=%d" % (m, n, k))
 
 
-# Shapes with few row tiles and many 1024-column chunks run as a cluster of K parts (2 CTAs
-# for (300, 8192) and (37, 6144, group 256), 3 with a partial last chunk for (40, 9856), 8 for
-# (100, 24576)); the down projection [5120, 17408] is the full-size case.
+# Shapes with few row tiles and long rows: the FP16 kernel's 2048-column chunks where its
+# activation table fits (one 3-D request per chunk; 2-D boxes and a ragged last chunk of 13
+# blocks for k = 9856), else (k = 24576 at m = 8) the BF16 kernel with its cluster K split;
+# the down projection [5120, 17408] is the full-size case.
 @pytest.mark.parametrize("m", [1, 3, 8])
 @pytest.mark.parametrize("n,k,group", [(300, 8192, 128), (37, 6144, 256), (40, 9856, 128), (100, 24576, 128),
                                        (5120, 17408, 128)])
