@@ -258,6 +258,10 @@ __global__ void __launch_bounds__(Q8T, Q8_CTAS_PER_SM)
     }
     fence_barrier_init();
     __syncthreads();
+    // programmatic dependent launch: the set-up above may overlap the previous kernel on the
+    // stream; x and the output are touched only once that kernel has completed
+    pdl_wait();
+    pdl_launch_dependents();
     if (warp == Q8C / 32) {
         if (lane == 0) q8_produce(x, stage, full, empty, total);
         return;
@@ -616,8 +620,19 @@ int quantize_act_q8_1(const uint16_t* x, void* act_q8, uint32_t m, uint32_t k, b
                 return fail(BQ_ERR_LAUNCH, "quantize_act_q8_1: cannot reserve %d bytes of shared memory", Q8_SMEM);
             configured[dev] = 1;
         }
-        q8_1_block_kernel<<<(unsigned)(units < cap ? units : cap), Q8T, Q8_SMEM, (cudaStream_t)stream>>>(x, codes, ds,
-                                                                                                     total);
+        // launched with programmatic stream serialization: its CTAs may start while the previous
+        // kernel drains and wait (griddepcontrol) before they touch memory
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(units < cap ? units : cap));
+        cfg.blockDim = dim3(Q8T);
+        cfg.dynamicSmemBytes = Q8_SMEM;
+        cfg.stream = (cudaStream_t)stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaLaunchKernelEx(&cfg, q8_1_block_kernel, x, codes, ds, (int64_t)total);
         return check_launch("quantize_act_q8_1");
     }
     const int64_t work = (int64_t)m * kp / 8;
