@@ -75,11 +75,52 @@ __global__ void __launch_bounds__(256) q2_dequant_kernel(const uint8_t* __restri
     }
 }
 
+// q8_1 helpers (their arithmetic is explained above q8_1_block_kernel below).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Four codes with magnitudes c (0..127, the low byte of each of m0..m3) and the signs of the
+// BF16 values in bytes 1 and 3 of w0 and w1, as one word of int8 codes.  Each sign byte is
+// 0x00 or 0xFF (prmt's sign-replicating selector); -c per byte is ((c ^ 0xFF) & 0x7F) + 1
+// with the top bit flipped, which never carries into the next byte (c = 0 gives 0x80 ^ 0x80).
+__device__ __forceinline__ uint32_t q8_pack4(uint32_t m0, uint32_t m1, uint32_t m2, uint32_t m3, uint32_t w0,
+                                             uint32_t w1) {
+    const uint32_t mag = prmt(prmt(m0, m1, 0x0040u), prmt(m2, m3, 0x0040u), 0x5410u);
+    const uint32_t sgn = prmt(w0, w1, 0xFDB9u);
+    const uint32_t low = ((mag ^ sgn) & 0x7F7F7F7Fu) + (sgn & 0x01010101u);
+    return low ^ (sgn & 0x80808080u);
+}
+
+// 2^23 + |code| as float bits, by IEEE division (any d > 0): floor(RZ(|y| + 1/2)) equals
+// floor(|y| + 1/2) because the integers are representable; clamped to 127.
+__device__ __forceinline__ uint32_t q8_mag_div(float v, float d) {
+    const float a = fminf(__fadd_rz(fabsf(__fdiv_rn(v, d)), 0.5f), 127.0f);
+    return __float_as_uint(__fadd_rz(a, 8388608.0f));
+}
+
+// The same bits without a division per value (d normal, r = RN(1/d)).
+__device__ __forceinline__ uint32_t q8_mag_fast(float v, float d, float r) {
+    const float a = fabsf(v);
+    const float y0 = __fmul_rn(a, r);
+    const float y = __fmaf_rn(__fmaf_rn(-d, y0, a), r, y0);  // RN(a / d)
+    return __float_as_uint(__fadd_rz(__fadd_rz(y, 0.5f), 8388608.0f));
+}
+
+// RN(amax / 127) for a BF16 amax >= 2^-94.
+__device__ __forceinline__ float q8_scale(float amax) {
+    constexpr float c127 = 1.0f / 127.0f;
+    const float q0 = __fmul_rn(amax, c127);
+    return __fmaf_rn(__fmaf_rn(-q0, 127.0f, amax), c127, q0);
+}
+
 // =====================================================================================
 // q8_1 quantisation.  Thread -> 8 values; a quad of 4 threads owns one 32-value block.
-// d = amax/127, q = round-half-away(x/d), s = d*sum(q), every step an IEEE fp32
-// operation rounded to nearest (explicit _rn intrinsics, no contraction).  This form takes
-// any k (zero padding to kp); k % 256 == 0 goes to q8_1_block_kernel below.
+// d = RN(amax/127), q = round-half-away(RN(x/d)), s = RN(d*sum(q)), with the division-free
+// exact form of q8_1_block_kernel below (IEEE divisions for blocks with amax < 2^-94).  This
+// form takes any k (zero padding to kp); k % 256 == 0 goes to q8_1_block_kernel.
 // Source: q4k_mmq.rs, `quantize_act_q8_1`.
 // =====================================================================================
 template <bool VEC>
@@ -108,27 +149,31 @@ __global__ void __launch_bounds__(256) q8_1_kernel(const uint16_t* __restrict__ 
         for (int j = 0; j < 8; j++) amax = fmaxf(amax, fabsf(v[j]));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        const float d = __fdiv_rn(amax, 127.0f);
-        int q[8];
-        int sum = 0;
+        // the BF16 bit patterns of the eight values (their signs for the packing)
+        uint32_t wb[4];
 #pragma unroll
-        for (int j = 0; j < 8; j++) {
-            int t = 0;
+        for (int j = 0; j < 4; j++) wb[j] = (__float_as_uint(v[2 * j]) >> 16) | (__float_as_uint(v[2 * j + 1]) & 0xFFFF0000u);
+        float d;
+        uint32_t lo = 0, hi = 0;
+        if (amax >= 0x1p-94f) {
+            d = q8_scale(amax);
+            const float rc = __frcp_rn(d);
+            lo = q8_pack4(q8_mag_fast(v[0], d, rc), q8_mag_fast(v[1], d, rc), q8_mag_fast(v[2], d, rc),
+                          q8_mag_fast(v[3], d, rc), wb[0], wb[1]);
+            hi = q8_pack4(q8_mag_fast(v[4], d, rc), q8_mag_fast(v[5], d, rc), q8_mag_fast(v[6], d, rc),
+                          q8_mag_fast(v[7], d, rc), wb[2], wb[3]);
+        } else {
+            d = __fdiv_rn(amax, 127.0f);
             if (amax != 0.0f) {
-                t = (int)roundf(__fdiv_rn(v[j], d));
-                t = max(-127, min(127, t));
+                lo = q8_pack4(q8_mag_div(v[0], d), q8_mag_div(v[1], d), q8_mag_div(v[2], d), q8_mag_div(v[3], d),
+                              wb[0], wb[1]);
+                hi = q8_pack4(q8_mag_div(v[4], d), q8_mag_div(v[5], d), q8_mag_div(v[6], d), q8_mag_div(v[7], d),
+                              wb[2], wb[3]);
             }
-            q[j] = t;
-            sum += t;
         }
+        int sum = __dp4a((int)hi, 0x01010101, __dp4a((int)lo, 0x01010101, 0));
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
         sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        uint32_t lo = 0, hi = 0;
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-            lo |= (uint32_t)(q[j] & 0xFF) << (8 * j);
-            hi |= (uint32_t)(q[4 + j] & 0xFF) << (8 * j);
-        }
         *reinterpret_cast<uint2*>(codes + r * kp + c0) = make_uint2(lo, hi);
         if ((threadIdx.x & 3) == 0) ds[r * (kp / 32) + c0 / 32] = make_float2(d, __fmul_rn(d, (float)sum));
     }
@@ -176,46 +221,6 @@ constexpr int Q8C = Q8U / 32;           // consumer threads (one 32-value block 
 constexpr int Q8T = Q8C + 32;            // plus one producer warp
 constexpr int Q8_CTAS_PER_SM = 4;
 constexpr int Q8_SMEM = Q8S * Q8U * 2 + 2 * Q8S * 8;
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
-
-// Four codes with magnitudes c (0..127, the low byte of each of m0..m3) and the signs of the
-// BF16 values in bytes 1 and 3 of w0 and w1, as one word of int8 codes.  Each sign byte is
-// 0x00 or 0xFF (prmt's sign-replicating selector); -c per byte is ((c ^ 0xFF) & 0x7F) + 1
-// with the top bit flipped, which never carries into the next byte (c = 0 gives 0x80 ^ 0x80).
-__device__ __forceinline__ uint32_t q8_pack4(uint32_t m0, uint32_t m1, uint32_t m2, uint32_t m3, uint32_t w0,
-                                             uint32_t w1) {
-    const uint32_t mag = prmt(prmt(m0, m1, 0x0040u), prmt(m2, m3, 0x0040u), 0x5410u);
-    const uint32_t sgn = prmt(w0, w1, 0xFDB9u);
-    const uint32_t low = ((mag ^ sgn) & 0x7F7F7F7Fu) + (sgn & 0x01010101u);
-    return low ^ (sgn & 0x80808080u);
-}
-
-// 2^23 + |code| as float bits, by IEEE division (any d > 0): floor(RZ(|y| + 1/2)) equals
-// floor(|y| + 1/2) because the integers are representable; clamped to 127.
-__device__ __forceinline__ uint32_t q8_mag_div(float v, float d) {
-    const float a = fminf(__fadd_rz(fabsf(__fdiv_rn(v, d)), 0.5f), 127.0f);
-    return __float_as_uint(__fadd_rz(a, 8388608.0f));
-}
-
-// The same bits without a division per value (d normal, r = RN(1/d)).
-__device__ __forceinline__ uint32_t q8_mag_fast(float v, float d, float r) {
-    const float a = fabsf(v);
-    const float y0 = __fmul_rn(a, r);
-    const float y = __fmaf_rn(__fmaf_rn(-d, y0, a), r, y0);  // RN(a / d)
-    return __float_as_uint(__fadd_rz(__fadd_rz(y, 0.5f), 8388608.0f));
-}
-
-// RN(amax / 127) for a BF16 amax >= 2^-94.
-__device__ __forceinline__ float q8_scale(float amax) {
-    constexpr float c127 = 1.0f / 127.0f;
-    const float q0 = __fmul_rn(amax, c127);
-    return __fmaf_rn(__fmaf_rn(-q0, 127.0f, amax), c127, q0);
-}
 
 // Producer warp of the flat q8_1 kernels: one bulk copy per unit into the ring.
 __device__ __forceinline__ void q8_produce(const uint16_t* __restrict__ x, uint8_t (*stage)[Q8U * 2], uint64_t* full,
