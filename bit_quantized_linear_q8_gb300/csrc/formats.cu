@@ -637,7 +637,14 @@ int quantize_act_q8_1(const uint16_t* x, void* act_q8, uint32_t m, uint32_t k, b
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        cudaLaunchKernelEx(&cfg, q8_1_block_kernel, x, codes, ds, (int64_t)total);
+        const cudaError_t le = cudaLaunchKernelEx(&cfg, q8_1_block_kernel, x, codes, ds, (int64_t)total);
+        if (le != cudaSuccess) {
+            (void)cudaGetLastError();  // clear it: the failure is reported here
+            return fail(le == cudaErrorNoKernelImageForDevice || le == cudaErrorInvalidDeviceFunction
+                            ? BQ_ERR_UNSUPPORTED
+                            : BQ_ERR_LAUNCH,
+                        "quantize_act_q8_1: launch failed: %s", cudaGetErrorString(le));
+        }
         return check_launch("quantize_act_q8_1");
     }
     const int64_t work = (int64_t)m * kp / 8;
