@@ -96,7 +96,10 @@ int quantize_weight_q4k(const uint16_t* w, void* out_q4k, uint32_t n, uint32_t k
 /* ---------------------------------------------------------------- the hot path */
 
 /* q8_1 activation quantisation: BF16 x [m][k] -> act_q8 (bq_q8_1_bytes(m, k) bytes).
- * Bit-exact, fp32 decisions as described in the format section.
+ * Bit-exact, fp32 decisions as described in the format section.  For k % 256 == 0 the
+ * kernel is launched with programmatic stream serialization: its set-up may overlap the
+ * previous kernel on the stream, but it reads x and writes act_q8 only after that kernel
+ * has completed, so stream order holds as for any launch.
  * Source: q4k_mmq.rs, `quantize_act_q8_1` (k padded to 256). */
 int quantize_act_q8_1(const uint16_t* x, void* act_q8, uint32_t m, uint32_t k, bq_stream_t stream);
 
