@@ -134,6 +134,28 @@ def test_q8_1_block_scale_range(B):
     assert np.array_equal(out, O.quantize_q8_1(xb))
 
 
+def test_q8_1_after_gemv_on_one_stream(B):
+    """The q8_1 launch may start while the kernel before it on the stream drains (programmatic
+    dependent launch), and the decode GEMV lets its dependents start early; q8_1 must still read
+    the GEMV's finished output.  Five GEMV -> q8_1 pairs back to back on one stream, with no
+    synchronisation between them; each q8_1 result against the oracle's q8_1 of that GEMV
+    output, bit for bit."""
+    import torch
+    n, k, m = 4096, 5120, 4     # the GEMV's output rows [m, 4096] are q8_1's input (4096 % 256 == 0)
+    d = synth.small_q2(970, n, k, m)
+    w = dev_q2(B, d["codes"], d["scales"])
+    x = to_dev_u16_as_bf16(d["x"])
+    ys, acts = [], []
+    for i in range(5):
+        xi = x if i == 0 else (x * (1.0 + 0.25 * i)).contiguous()
+        y = B.q2_gemv_batchm(xi, w)
+        ys.append(y)
+        acts.append(B.quantize_act_q8_1(y))
+    torch.cuda.synchronize()
+    for y, a in zip(ys, acts):
+        assert np.array_equal(u8_dev(a), O.quantize_q8_1(bf16_dev_to_u16(y)))
+
+
 # ------------------------------------------------------------------------------ NVFP4 -> BF16
 def _nvfp4(B, d, scale2=None):
     import torch
