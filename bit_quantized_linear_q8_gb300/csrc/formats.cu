@@ -75,7 +75,27 @@ __global__ void __launch_bounds__(256) q2_dequant_kernel(const uint8_t* __restri
     }
 }
 
-// q8_1 helpers (their arithmetic is explained above q8_1_block_kernel below).
+// =====================================================================================
+// q8_1 arithmetic.  q8_1 (q4k_mmq.rs, `quantize_act_q8_1`) takes per 32-value block
+// d = RN(amax / 127), code = round-half-away(RN(x / d)) clamped to [-127, 127] and
+// s = RN(d * sum(code)), each an IEEE fp32 operation.
+// The kernels compute the same codes without a division per value:
+//  * RN(a / d) for a = |x| is Markstein's correction of y0 = RN(a r) with r = RN(1/d):
+//    RN(y0 + r RN(a - d y0)), two FMAs (P. Markstein, "Computation of elementary functions on
+//    the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990: with a correctly
+//    rounded reciprocal and a quotient within an ulp, one correction rounds correctly).
+//  * round-half-away of that y >= 0 is floor(RZ(y + 1/2)) (the integers are representable,
+//    so rounding the sum toward zero never crosses one), and a second round-toward-zero add
+//    of 2^23 leaves it in the low mantissa byte.
+//  * d = RN(amax / 127) from q0 = RN(amax c), c = RN(1/127), and one FMA correction of the
+//    exact residual amax - 127 q0.
+// Both forms are checked on the host against the IEEE divisions for every BF16 pair
+// |x| <= amax of several binades (tests/test_q8_1_arith.py); the quotient can differ only
+// where the residual underflows, for quotients below 2^-100 whose code is 0.  Scaling by
+// powers of two keeps all of it exact while d is normal, so blocks with amax >= 2^-94 take
+// this path and smaller ones the IEEE divisions.  The four code bytes of a word are gathered
+// with byte permutes and the signs applied to all four at once.
+// =====================================================================================
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -119,8 +139,8 @@ __device__ __forceinline__ float q8_scale(float amax) {
 // =====================================================================================
 // q8_1 quantisation.  Thread -> 8 values; a quad of 4 threads owns one 32-value block.
 // d = RN(amax/127), q = round-half-away(RN(x/d)), s = RN(d*sum(q)), with the division-free
-// exact form of q8_1_block_kernel below (IEEE divisions for blocks with amax < 2^-94).  This
-// form takes any k (zero padding to kp); k % 256 == 0 goes to q8_1_block_kernel.
+// exact form above (IEEE divisions for blocks with amax < 2^-94).  This form takes any k
+// (zero padding to kp); k % 256 == 0 goes to q8_1_block_kernel below.
 // Source: q4k_mmq.rs, `quantize_act_q8_1`.
 // =====================================================================================
 template <bool VEC>
@@ -186,25 +206,8 @@ __global__ void __launch_bounds__(256) q8_1_kernel(const uint16_t* __restrict__ 
 // a producer warp), so that the bytes in flight do not depend on the consumers' registers.
 // Units are 16 KB because a bulk request costs the SM a roughly fixed time (4 KB ones held
 // the whole GPU near 2.7 TB/s).  One consumer thread takes one 32-value block: its amax
-// from BF16 pair maxima, its codes, the sum of its codes by dp4a, and its (d, s) pair.
-//
-// The codes are those of the IEEE sequence above, code = round-half-away(RN(x / d)) with
-// d = RN(amax / 127), computed without a division per value:
-//  * RN(a / d) for a = |x| is Markstein's correction of y0 = RN(a r) with r = RN(1/d):
-//    RN(y0 + r RN(a - d y0)), two FMAs (P. Markstein, "Computation of elementary functions on
-//    the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990: with a correctly
-//    rounded reciprocal and a quotient within an ulp, one correction rounds correctly).
-//  * round-half-away of that y >= 0 is floor(RZ(y + 1/2)) (the integers are representable,
-//    so rounding the sum toward zero never crosses one), and a second round-toward-zero add
-//    of 2^23 leaves it in the low mantissa byte.
-//  * d = RN(amax / 127) from q0 = RN(amax c), c = RN(1/127), and one FMA correction of the
-//    exact residual amax - 127 q0.
-// Both forms are checked on the host against the IEEE divisions for every BF16 pair
-// |x| <= amax of several binades (tests/test_q8_1_arith.py); the quotient can differ only
-// where the residual underflows, for quotients below 2^-100 whose code is 0.  Scaling by
-// powers of two keeps all of it exact while d is normal, so blocks with amax >= 2^-94 take
-// this path and smaller ones the IEEE divisions.  The four code bytes of a word are gathered
-// with byte permutes and the signs applied to all four at once.
+// from BF16 pair maxima, its codes (the exact arithmetic above), the sum of its codes by
+// dp4a, and its (d, s) pair.
 // -------------------------------------------------------------------------------------
 static __device__ unsigned int g_q8_status;
 

@@ -1,6 +1,6 @@
 """Host check of the arithmetic the flat q8_1 kernel uses in place of IEEE divisions.
 
-The kernel (formats.cu, q8_1_block_kernel) takes d = RN(amax / 127) as RN(q0 + c RN(amax - 127 q0))
+The q8_1 kernels (formats.cu) take d = RN(amax / 127) as RN(q0 + c RN(amax - 127 q0))
 with q0 = RN(amax c), c = RN(1/127), and each code from y = RN(y0 + r RN(a - d y0)), y0 = RN(a r),
 r = RN(1/d), as floor(RZ(y + 1/2)).  The q8_1 definition (q4k_mmq.rs, `quantize_act_q8_1`) asks
 for d = RN(amax / 127) and code = round-half-away(RN(x / d)).  Here both are evaluated on the
