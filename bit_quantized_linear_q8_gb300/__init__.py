@@ -10,6 +10,7 @@ init_q2.rs `qkvz_q2_prefill_gemm`, q4k_mmq.rs `q4k_mmq_gemm`).  BF16 tensors are
 ``torch.bfloat16``; packed weights and q8_1 buffers are ``torch.uint8``.
 """
 import ctypes
+import functools
 from dataclasses import dataclass
 
 from . import _abi
@@ -29,11 +30,25 @@ def _torch():
 
 
 def _ptr(t):
-    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+    # the C signatures declare void*, so ctypes converts the int (None is NULL)
+    return t.data_ptr() if t is not None else None
+
+
+_raw_stream = None
 
 
 def _stream():
-    return ctypes.c_void_p(_torch().cuda.current_stream().cuda_stream)
+    """The current CUDA stream of the current device, as a handle for the C ABI."""
+    global _raw_stream
+    if _raw_stream is None:
+        torch = _torch()
+        get_raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        get_dev = getattr(torch._C, "_cuda_getDevice", None)
+        if get_raw is not None and get_dev is not None:
+            _raw_stream = lambda: get_raw(get_dev())  # noqa: E731  (no Stream object per call)
+        else:
+            _raw_stream = lambda: torch.cuda.current_stream().cuda_stream  # noqa: E731
+    return _raw_stream()
 
 
 def _need(t, dtype, name, shape=None):
@@ -59,10 +74,12 @@ def _need_bytes(t, nbytes, name):
     return t
 
 
+@functools.lru_cache(maxsize=256)
 def q2_weight_bytes(n: int, k: int, group: int = 128) -> int:
     return int(lib().bq_q2_weight_bytes(n, k, group))
 
 
+@functools.lru_cache(maxsize=256)
 def q8_1_bytes(m: int, k: int) -> int:
     return int(lib().bq_q8_1_bytes(m, k))
 
@@ -80,8 +97,18 @@ class Q2Weight:
     group: int = 128
 
     def desc(self):
-        _need_bytes(self.data, q2_weight_bytes(self.n, self.k, self.group), "Q2Weight.data")
-        return _abi.Q2WeightDesc(self.data.data_ptr(), self.n, self.k, self.group)
+        """The C struct for this weight; checked and built again whenever the tensor or the
+        shape fields change."""
+        t = self.data
+        key = (id(t), t.data_ptr() if hasattr(t, "data_ptr") else None, getattr(t, "dtype", None),
+               getattr(t, "shape", None), self.n, self.k, self.group)
+        cached = self.__dict__.get("_desc")
+        if cached is not None and cached[0] == key:
+            return cached[1]
+        _need_bytes(t, q2_weight_bytes(self.n, self.k, self.group), "Q2Weight.data")
+        d = _abi.Q2WeightDesc(t.data_ptr(), self.n, self.k, self.group)
+        self.__dict__["_desc"] = (key, d)
+        return d
 
 
 def q2_pack(codes, scales, group: int = 128) -> Q2Weight:
