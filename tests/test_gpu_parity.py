@@ -332,6 +332,25 @@ def test_gemv_qkvz_full(B, m):
     assert y.shape == (m, d["n_qkv"] + d["n_z"])
 
 
+def test_gemv_weight_descriptor_follows_the_tensor(B):
+    """The binding keeps each weight's checked C descriptor between calls; replacing the
+    weight's tensor or its shape fields must rebuild (and re-check) it."""
+    import torch
+    n, k, m = 64, 512, 2
+    d1 = synth.small_q2(480, n, k, m)
+    d2 = synth.small_q2(481, n, k, m)
+    w = dev_q2(B, d1["codes"], d1["scales"])
+    x = to_dev_u16_as_bf16(d1["x"])
+    y1 = bf16_dev_to_u16(B.q2_gemv_batchm(x, w))
+    check_bf16_vs_f64(y1, O.q2_gemv(d1["x"], O.q2_pack(d1["codes"], d1["scales"]), n, k), "first weight")
+    w.data = dev_q2(B, d2["codes"], d2["scales"]).data          # another tensor, same shape
+    y2 = bf16_dev_to_u16(B.q2_gemv_batchm(x, w))
+    check_bf16_vs_f64(y2, O.q2_gemv(d1["x"], O.q2_pack(d2["codes"], d2["scales"]), n, k), "replaced weight")
+    w.n = 2 * n                                                  # too few bytes for the new shape
+    with pytest.raises(ValueError):
+        B.q2_gemv_batchm(x, w)
+
+
 def test_gemv_edge_shapes(B):
     import torch
     from bit_quantized_linear_q8_gb300 import Q2Weight
