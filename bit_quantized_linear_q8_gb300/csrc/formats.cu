@@ -416,50 +416,65 @@ __device__ __forceinline__ void nv_word_lookup(uint32_t w, uint32_t lo0, uint32_
 // so two exactly rounded values b1 = BF16(Q) and b3 = BF16(1.5 Q) give all eight magnitudes
 // by exponent adds (exact while the results stay normal BF16 numbers); groups where they
 // would not (zero, huge or tiny Q, a NaN scale) take the per-value path.
+// One group: 16 values from their 8 code bytes c and E4M3 scale byte, stored as 32 bytes.
+__device__ __forceinline__ void nvfp4_group(uint2 c, uint32_t sbyte, float scale2, uint16_t* __restrict__ out) {
+    const float sc = nv_e4m3(sbyte);
+    uint32_t o[8];
+    uint32_t t1, t3;
+    const uint32_t b1 = nv_bf16_fast(sc, scale2, t1);
+    const uint32_t b3 = nv_bf16_fast(1.5f * sc, scale2, t3);  // 1.5 sc is exact
+    const uint32_t e1 = (b1 >> 7) & 0xFFu, e3 = (b3 >> 7) & 0xFFu;
+    if ((t1 | t3) == 0u && e1 >= 2u && e1 <= 252u && e3 >= 1u && e3 <= 252u) {
+        // T = (+-0, Q/2, Q, 1.5Q, 2Q, 3Q, 4Q, 6Q) as BF16, the zero with Q's sign
+        const uint32_t p01 = (b1 & 0x8000u) | ((b1 - 128u) << 16), p23 = b1 | (b3 << 16);
+        const uint32_t p45 = (b1 + 128u) | ((b3 + 128u) << 16), p67 = (b1 + 256u) | ((b3 + 256u) << 16);
+        const uint32_t lo0 = __byte_perm(p01, p23, 0x6420u), hi0 = __byte_perm(p01, p23, 0x7531u);
+        const uint32_t lo1 = __byte_perm(p45, p67, 0x6420u), hi1 = __byte_perm(p45, p67, 0x7531u);
+        nv_word_lookup(c.x, lo0, lo1, hi0, hi1, o);
+        nv_word_lookup(c.y, lo0, lo1, hi0, hi1, o + 4);
+    } else {
+        float a[16];
+        uint32_t tiny = 0;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const uint32_t byte = ((j < 4 ? c.x : c.y) >> (8 * (j & 3))) & 0xFFu;
+            a[2 * j] = nv_e2m1(byte & 15u) * sc;  // exact
+            a[2 * j + 1] = nv_e2m1(byte >> 4) * sc;
+            uint32_t u0, u1;
+            o[j] = nv_bf16_fast(a[2 * j], scale2, u0) | (nv_bf16_fast(a[2 * j + 1], scale2, u1) << 16);
+            tiny |= (u0 << (2 * j)) | (u1 << (2 * j + 1));
+        }
+#pragma unroll
+        for (int e = 0; e < 16; e++) {  // products near the BF16 subnormal range, exactly
+            if ((tiny >> e) & 1u) {
+                const uint32_t v = nv_bf16_exact(a[e], scale2);
+                o[e >> 1] = (e & 1) ? ((o[e >> 1] & 0xFFFFu) | (v << 16)) : ((o[e >> 1] & 0xFFFF0000u) | v);
+            }
+        }
+    }
+    uint4* dst = reinterpret_cast<uint4*>(out);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// Two groups a thread per step (g and g + stride), both groups' loads issued first.
 __global__ void __launch_bounds__(256) nvfp4_dequant_kernel(const uint8_t* __restrict__ packed,
                                                             const uint8_t* __restrict__ scales,
                                                             uint16_t* __restrict__ out, float scale2,
                                                             int64_t ngroups) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < ngroups; g += stride) {
-        const uint2 c = __ldg(reinterpret_cast<const uint2*>(packed + 8 * g));
-        const float sc = nv_e4m3(__ldg(scales + g));
-        uint32_t o[8];
-        uint32_t t1, t3;
-        const uint32_t b1 = nv_bf16_fast(sc, scale2, t1);
-        const uint32_t b3 = nv_bf16_fast(1.5f * sc, scale2, t3);  // 1.5 sc is exact
-        const uint32_t e1 = (b1 >> 7) & 0xFFu, e3 = (b3 >> 7) & 0xFFu;
-        if ((t1 | t3) == 0u && e1 >= 2u && e1 <= 252u && e3 >= 1u && e3 <= 252u) {
-            // T = (+-0, Q/2, Q, 1.5Q, 2Q, 3Q, 4Q, 6Q) as BF16, the zero with Q's sign
-            const uint32_t p01 = (b1 & 0x8000u) | ((b1 - 128u) << 16), p23 = b1 | (b3 << 16);
-            const uint32_t p45 = (b1 + 128u) | ((b3 + 128u) << 16), p67 = (b1 + 256u) | ((b3 + 256u) << 16);
-            const uint32_t lo0 = __byte_perm(p01, p23, 0x6420u), hi0 = __byte_perm(p01, p23, 0x7531u);
-            const uint32_t lo1 = __byte_perm(p45, p67, 0x6420u), hi1 = __byte_perm(p45, p67, 0x7531u);
-            nv_word_lookup(c.x, lo0, lo1, hi0, hi1, o);
-            nv_word_lookup(c.y, lo0, lo1, hi0, hi1, o + 4);
-        } else {
-            float a[16];
-            uint32_t tiny = 0;
-#pragma unroll
-            for (int j = 0; j < 8; j++) {
-                const uint32_t byte = ((j < 4 ? c.x : c.y) >> (8 * (j & 3))) & 0xFFu;
-                a[2 * j] = nv_e2m1(byte & 15u) * sc;  // exact
-                a[2 * j + 1] = nv_e2m1(byte >> 4) * sc;
-                uint32_t u0, u1;
-                o[j] = nv_bf16_fast(a[2 * j], scale2, u0) | (nv_bf16_fast(a[2 * j + 1], scale2, u1) << 16);
-                tiny |= (u0 << (2 * j)) | (u1 << (2 * j + 1));
-            }
-#pragma unroll
-            for (int e = 0; e < 16; e++) {  // products near the BF16 subnormal range, exactly
-                if ((tiny >> e) & 1u) {
-                    const uint32_t v = nv_bf16_exact(a[e], scale2);
-                    o[e >> 1] = (e & 1) ? ((o[e >> 1] & 0xFFFFu) | (v << 16)) : ((o[e >> 1] & 0xFFFF0000u) | v);
-                }
-            }
+    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < ngroups; g += 2 * stride) {
+        const int64_t g2 = g + stride;
+        const uint2 c1 = __ldg(reinterpret_cast<const uint2*>(packed + 8 * g));
+        const uint32_t s1 = __ldg(scales + g);
+        uint2 c2 = make_uint2(0u, 0u);
+        uint32_t s2 = 0;
+        if (g2 < ngroups) {
+            c2 = __ldg(reinterpret_cast<const uint2*>(packed + 8 * g2));
+            s2 = __ldg(scales + g2);
         }
-        uint4* dst = reinterpret_cast<uint4*>(out + 16 * g);
-        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        nvfp4_group(c1, s1, scale2, out + 16 * g);
+        if (g2 < ngroups) nvfp4_group(c2, s2, scale2, out + 16 * g2);
     }
 }
 
