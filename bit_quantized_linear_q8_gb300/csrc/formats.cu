@@ -43,6 +43,29 @@ __global__ void q2_pack_kernel(const uint8_t* __restrict__ codes, const uint16_t
 // d*(c-2) exactly (both steps are exact in BF16).
 // Source: init_q2.rs, `qkvz_q2_prefill_gemm` fallback (`dequant_q2_0_gn_to_bf16`).
 // =====================================================================================
+// One 8-byte quarter of a pack block (32 codes: 4 runs of 8 consecutive columns) to BF16.
+__device__ __forceinline__ void q2_dequant_quarter(uint2 w, float d, uint16_t* __restrict__ dst) {
+    const __nv_bfloat162 c15 = __floats2bfloat162_rn(1.5f, 1.5f);
+    const __nv_bfloat162 d4 = __floats2bfloat162_rn(4.0f * d, 4.0f * d);
+    // bytes (b, b+1) into the low byte of each 16-bit half
+    const uint32_t e[4] = {__byte_perm(w.x, 0, 0x4140), __byte_perm(w.x, 0, 0x4342), __byte_perm(w.y, 0, 0x4140),
+                           __byte_perm(w.y, 0, 0x4342)};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const uint32_t s = (i < 3) ? (e[j] << (5 - 2 * i)) : (e[j] >> 1);
+            const uint32_t v = (s & 0x00600060u) | 0x3F803F80u;
+            o[j] = bf162_bits(__hmul2(__hsub2(bits_bf162(v), c15), d4));
+        }
+        *reinterpret_cast<uint4*>(dst + 32 * i) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// Two quarters a thread per step (id and id + stride), both quarters' loads issued first.
+// Quarter id is row id / (k/32), quarter id % (k/32) of the row (32-bit division when every
+// index fits).
 __global__ void __launch_bounds__(256) q2_dequant_kernel(const uint8_t* __restrict__ packed, uint16_t* __restrict__ out,
                                                          int64_t n, int64_t k, int group) {
     const int64_t q_per_row = k / 32;  // 8-byte quarters of pack blocks per row
@@ -50,28 +73,32 @@ __global__ void __launch_bounds__(256) q2_dequant_kernel(const uint8_t* __restri
     const int64_t groups = k / group;
     const uint16_t* sc = reinterpret_cast<const uint16_t*>(packed + n * (k / 4));
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    const __nv_bfloat162 c15 = __floats2bfloat162_rn(1.5f, 1.5f);
-    for (int64_t id = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; id < total; id += stride) {
-        const int64_t r = id / q_per_row, qi = id % q_per_row;
-        const int64_t p = qi / 4, l0 = (qi % 4) * 8;
-        const uint2 w = ldg_stream64(packed + r * (k / 4) + p * 32 + l0);
-        const float d = bf16_bits_to_f32(sc[r * groups + (p * 128) / group]);
-        const __nv_bfloat162 d4 = __floats2bfloat162_rn(4.0f * d, 4.0f * d);
-        // bytes (b, b+1) into the low byte of each 16-bit half
-        const uint32_t e[4] = {__byte_perm(w.x, 0, 0x4140), __byte_perm(w.x, 0, 0x4342), __byte_perm(w.y, 0, 0x4140),
-                               __byte_perm(w.y, 0, 0x4342)};
-        uint16_t* dst = out + r * k + p * 128 + l0;
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            uint32_t o[4];
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-                const uint32_t s = (i < 3) ? (e[j] << (5 - 2 * i)) : (e[j] >> 1);
-                const uint32_t v = (s & 0x00600060u) | 0x3F803F80u;
-                o[j] = bf162_bits(__hmul2(__hsub2(bits_bf162(v), c15), d4));
-            }
-            *reinterpret_cast<uint4*>(dst + 32 * i) = make_uint4(o[0], o[1], o[2], o[3]);
+    const bool idx32 = total + 2 * stride <= 0xFFFFFFFFll;
+    auto split = [&](int64_t id, int64_t& r, int64_t& qi) {
+        if (idx32) {
+            const uint32_t u = (uint32_t)id, qpr = (uint32_t)q_per_row;
+            r = u / qpr;
+            qi = u - (uint32_t)r * qpr;
+        } else {
+            r = id / q_per_row;
+            qi = id - r * q_per_row;
         }
+    };
+    for (int64_t id = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; id < total; id += 2 * stride) {
+        const int64_t id2 = id + stride;
+        int64_t r1, q1, r2 = 0, q2 = 0;
+        split(id, r1, q1);
+        const uint2 w1 = ldg_stream64(packed + r1 * (k / 4) + (q1 >> 2) * 32 + (q1 & 3) * 8);
+        const uint16_t s1 = sc[r1 * groups + ((uint32_t)(q1 >> 2) * 128u) / (uint32_t)group];
+        uint2 w2 = make_uint2(0u, 0u);
+        uint16_t s2 = 0;
+        if (id2 < total) {
+            split(id2, r2, q2);
+            w2 = ldg_stream64(packed + r2 * (k / 4) + (q2 >> 2) * 32 + (q2 & 3) * 8);
+            s2 = sc[r2 * groups + ((uint32_t)(q2 >> 2) * 128u) / (uint32_t)group];
+        }
+        q2_dequant_quarter(w1, bf16_bits_to_f32(s1), out + r1 * k + (q1 >> 2) * 128 + (q1 & 3) * 8);
+        if (id2 < total) q2_dequant_quarter(w2, bf16_bits_to_f32(s2), out + r2 * k + (q2 >> 2) * 128 + (q2 & 3) * 8);
     }
 }
 
