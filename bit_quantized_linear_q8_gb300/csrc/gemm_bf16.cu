@@ -277,16 +277,19 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
 using namespace bq8;
 
 // ---------------------------------------------------------------------------------------
-// The CTA-pair form (m > 128): a cluster of two CTAs computes a 256 x 256 output tile with
-// tcgen05.mma.cta_group::2 M256 N256 K16, issued by the even CTA.  CTA r of the pair holds
-// rows 128 r .. 128 r + 127 of the tile's activations and of its weight rows (the MMA's B
-// operand is split along N across the pair), both at the same shared-memory offsets, and
-// receives its 128 output rows x 256 columns in its own tensor memory.  Per K step each CTA
-// stages 16 KB + 16 KB instead of 16 + 32 KB for a 128 x 256 tile, so the operand traffic
-// through each SM's shared memory per MMA is a third lower.
-//  * Each CTA's producer lane streams its own halves through a six-stage ring; both CTAs' copies
-//    complete their bytes on the even CTA's `full` barrier (the cta_group::2 form of the TMA
-//    load), whose one arrival expects the pair's 64 KB per stage.
+// The CTA-pair form (m > 128): a cluster of two CTAs computes a 256 x 256 NB output tile (NB = 1
+// or 2) with tcgen05.mma.cta_group::2 M256 N256 K16, NB MMAs per K16 step sharing the
+// activation operand, issued by the even CTA.  CTA r of the pair holds rows 128 r .. 128 r + 127
+// of the tile's activations and, for MMA h, weight rows 256 h + 128 r .. + 127 (the MMA's B
+// operand is split along N across the pair), all at the same shared-memory offsets in both
+// CTAs, and receives its 128 output rows x 256 NB columns in its own tensor memory.  Per K step
+// each CTA stages 16 KB + 16 NB KB instead of 16 + 32 KB for a 128 x 256 tile, so the operand
+// traffic through each SM's shared memory per MMA is a third lower (NB = 1) or half (NB = 2).
+//  * Each CTA's producer lane streams its own halves through a ring (six stages, four at
+//    NB = 2); both CTAs' copies complete their bytes on the even CTA's `full` barrier (the
+//    cta_group::2 form of the TMA load), whose one arrival expects the pair's bytes per stage.
+//  * NB = 1 keeps two accumulator buffers in tensor memory, so a tile's epilogue overlaps the
+//    next tile's main loop; at NB = 2 the one 512-column accumulator is read out between tiles.
 //  * The even CTA's MMA lane commits each K step to the `empty` barriers of both CTAs and each
 //    tile's last step to both CTAs' accumulator barriers (multicast commits); both CTAs'
 //    epilogue warps read their lanes and arrive (the odd CTA's remotely) on the even CTA's
@@ -294,16 +297,25 @@ using namespace bq8;
 //  * Tensor memory is allocated and freed for the pair (cta_group::2, one warp in each CTA).
 //  * Every wait is bounded; both CTAs reach the final cluster barrier on every path.
 constexpr int GP_BM = 128;                              // rows per CTA (256 per pair)
-constexpr int GP_BN = 256;                              // output columns per pair tile
-constexpr int GP_NS = 6;
+constexpr int GP_BN = 256;                              // output columns per MMA (N)
 constexpr uint32_t GP_ASTAGE = GP_BM * GB_BK * 2;      // 16 KB
-constexpr uint32_t GP_BSTAGE = (GP_BN / 2) * GB_BK * 2;  // 16 KB: this CTA's half of the weight rows
-constexpr uint32_t GP_STAGE = GP_ASTAGE + GP_BSTAGE;
-constexpr size_t GP_SMEM = 1024 + (size_t)GP_NS * GP_STAGE + (2 * GP_NS + 5) * 8 + 16;
-static_assert(GP_SMEM <= 227 * 1024, "shared memory budget");
+constexpr uint32_t GP_BSTAGE = (GP_BN / 2) * GB_BK * 2;  // 16 KB: this CTA's half of one MMA's weight rows
 // D fp32, A and B BF16, both K-major, N = 256, M = 256 (the pair)
 constexpr uint32_t GP_IDESC =
     (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(GP_BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+// A pair tile is 256 x 256 NB: NB MMAs of N = 256 per K16 step share the activation operand.
+// NB = 1: six stages of 32 KB and two accumulator buffers (the epilogue of one tile overlaps
+// the next tile's main loop).  NB = 2: four stages of 48 KB and one 512-column accumulator;
+// a quarter fewer operand bytes per MMA, the epilogue not overlapped.
+template <int NB>
+struct GpCfg {
+    static constexpr int NS = NB == 1 ? 6 : 4;
+    static constexpr int NBUF = NB == 1 ? 2 : 1;  // accumulator buffers of 256 NB columns
+    static constexpr uint32_t STAGE = GP_ASTAGE + NB * GP_BSTAGE;
+    static constexpr size_t SMEM = 1024 + (size_t)NS * STAGE + (2 * NS + 5) * 8 + 16;
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+    static_assert(NBUF * NB * GP_BN <= GB_TMEM_COLS, "tensor memory budget");
+};
 
 __device__ __forceinline__ uint32_t gp_cluster_addr(const void* p, uint32_t rank) {
     uint32_t r;
@@ -353,11 +365,14 @@ __device__ __forceinline__ bool gp_wait(uint64_t* bar, uint32_t parity, volatile
     return false;
 }
 
+template <int NB>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GB_THREADS, 1)
     gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapW,
                           uint16_t* __restrict__ out, int m, int n, int k, int ntm, int ntiles) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* stages = align1024(smem_raw);  // [stage][a 128 x 64 | w 128 x 64] BF16, 128-byte swizzle
+    constexpr int GP_NS = GpCfg<NB>::NS, NBUF = GpCfg<NB>::NBUF;
+    constexpr uint32_t GP_STAGE = GpCfg<NB>::STAGE;
+    uint8_t* stages = align1024(smem_raw);  // [stage][a 128 x 64 | NB x w 128 x 64] BF16, 128-byte swizzle
     uint64_t* full = reinterpret_cast<uint64_t*>(stages + GP_NS * GP_STAGE);
     uint64_t* empty = full + GP_NS;
     uint64_t* accf = empty + GP_NS;  // [2] accumulator buffer holds a finished tile (both CTAs)
@@ -372,7 +387,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GB_THREADS, 1)
     const int S = k / GB_BK;
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
     auto tile_m0 = [&](int id) { return (id % ntm) * (2 * GP_BM); };
-    auto tile_n0 = [&](int id) { return (id / ntm) * GP_BN; };
+    auto tile_n0 = [&](int id) { return (id / ntm) * (GP_BN * NB); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < GP_NS; s++) {
@@ -416,7 +431,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GB_THREADS, 1)
                     const uint32_t bar = gp_cluster_addr(&full[st], 0);
                     if (rank == 0) mbar_arrive_expect_tx(&full[st], 2 * GP_STAGE);
                     gp_tma_load_2d(dst, &mapA, ks * GB_BK * 2, ma0, bar);
-                    gp_tma_load_2d(dst + GP_ASTAGE, &mapW, ks * GB_BK * 2, nb0, bar);
+#pragma unroll
+                    for (int h = 0; h < NB; h++)  // MMA h's weight rows: output columns n0 + 256 h ..
+                        gp_tma_load_2d(dst + GP_ASTAGE + h * GP_BSTAGE, &mapW, ks * GB_BK * 2, nb0 + GP_BN * h, bar);
                 }
             }
             // wind down (even CTA): the last copies of both CTAs land before the pair passes its
@@ -433,10 +450,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GB_THREADS, 1)
             bool ok = true;
             int ti = 0;
             for (int id = pair; id < ntiles && ok; id += npairs, ti++) {
-                const int buf = ti & 1;
-                if (ti >= 2 && !gp_wait(&acce[buf], (uint32_t)((ti >> 1) - 1) & 1u, abort)) break;
+                const int buf = ti % NBUF;
+                if (ti >= NBUF && !gp_wait(&acce[buf], (uint32_t)((ti / NBUF) - 1) & 1u, abort)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t d = tbase + (uint32_t)(buf * GP_BN);
+                const uint32_t d = tbase + (uint32_t)(buf * GP_BN * NB);
                 for (int ks = 0; ks < S; ks++, it++) {
                     const int st = (int)(it % GP_NS);
                     if (!gb_wait(&full[st], (uint32_t)(it / GP_NS) & 1u, abort)) {
@@ -448,11 +465,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GB_THREADS, 1)
                     const uint32_t bbase = abase + GP_ASTAGE;
 #pragma unroll
                     for (int kk = 0; kk < GB_BK / 16; kk++)
-                        asm volatile(
-                            "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
-                            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-                            "l"(gb_desc(abase + 32u * kk)), "l"(gb_desc(bbase + 32u * kk)), "r"(GP_IDESC),
-                            "r"((uint32_t)(ks | kk)));
+#pragma unroll
+                        for (int h = 0; h < NB; h++)
+                            asm volatile(
+                                "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
+                                "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d + GP_BN * h),
+                                "l"(gb_desc(abase + 32u * kk)), "l"(gb_desc(bbase + GP_BSTAGE * h + 32u * kk)),
+                                "r"(GP_IDESC), "r"((uint32_t)(ks | kk)));
                     gp_commit_pair(&empty[st]);  // both CTAs' stage is free once these MMAs have read it
                 }
                 gp_commit_pair(&accf[buf]);  // both CTAs' accumulator rows are complete
@@ -469,16 +488,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GB_THREADS, 1)
         const uint32_t acce_addr0 = gp_cluster_addr(&acce[0], 0), acce_addr1 = gp_cluster_addr(&acce[1], 0);
         int ti = 0;
         for (int id = pair; id < ntiles; id += npairs, ti++) {
-            const int buf = ti & 1;
-            bool ok = gb_wait(&accf[buf], (uint32_t)(ti >> 1) & 1u, abort);
+            const int buf = ti % NBUF;
+            bool ok = gb_wait(&accf[buf], (uint32_t)(ti / NBUF) & 1u, abort);
             ok = __all_sync(0xffffffffu, ok && !*abort) != 0;
             if (!ok) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const int m0 = tile_m0(id) + GP_BM * (int)rank, n0 = tile_n0(id);
             const int row = m0 + 32 * qd + lane;
-            const uint32_t tq = tbase + ((uint32_t)(32 * qd) << 16) + (uint32_t)(buf * GP_BN);
+            const uint32_t tq = tbase + ((uint32_t)(32 * qd) << 16) + (uint32_t)(buf * GP_BN * NB);
 #pragma unroll 1
-            for (int c = 0; c < GP_BN / 32; c++) {
+            for (int c = 0; c < GP_BN * NB / 32; c++) {
                 const int col0 = n0 + 32 * c;
                 if (col0 >= n) break;  // warp-uniform
                 uint32_t v[32];
@@ -521,29 +540,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GB_THREADS, 1)
     }
 }
 
-// The CTA-pair form for m > 128: one pair per two SMs walks the 256 x 256 tiles.
-static int launch_pair(const uint16_t* a, const uint16_t* w, uint16_t* out, uint32_t m, uint32_t n, uint32_t k,
-                       cudaStream_t stream, int dev, const char* who) {
+// The CTA-pair form for m > 128: one pair per two SMs walks the 256 x 256 NB tiles.
+template <int NB>
+static int launch_pair_nb(const uint16_t* a, const uint16_t* w, uint16_t* out, uint32_t m, uint32_t n, uint32_t k,
+                          cudaStream_t stream, int dev, const char* who) {
     static int configured[64] = {};
+    constexpr size_t smem = GpCfg<NB>::SMEM;
     if (!configured[dev]) {
-        if (cudaFuncSetAttribute(gemm_bf16_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GP_SMEM) !=
+        if (cudaFuncSetAttribute(gemm_bf16_pair_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
-            return fail(BQ_ERR_LAUNCH, "%s: cannot reserve %zu bytes of shared memory", who, GP_SMEM);
+            return fail(BQ_ERR_LAUNCH, "%s: cannot reserve %zu bytes of shared memory", who, smem);
         configured[dev] = 1;
     }
     CUtensorMap ma, mw;
     int st = cached_tmap_2d_u8(&ma, a, (uint64_t)k * 2, m, (uint64_t)k * 2, 128, GP_BM, true, who);
     if (st) return st;
     if ((st = cached_tmap_2d_u8(&mw, w, (uint64_t)k * 2, n, (uint64_t)k * 2, 128, GP_BN / 2, true, who))) return st;
-    const uint64_t ntiles64 = (uint64_t)((m + 2 * GP_BM - 1) / (2 * GP_BM)) * ((n + GP_BN - 1) / GP_BN);
+    const uint64_t ntiles64 = (uint64_t)((m + 2 * GP_BM - 1) / (2 * GP_BM)) * ((n + GP_BN * NB - 1) / (GP_BN * NB));
     if (ntiles64 >= (1ull << 31)) return fail(BQ_ERR_INVALID, "%s: too many output tiles", who);
     const int ntm = (int)((m + 2 * GP_BM - 1) / (2 * GP_BM));
     const int ntiles = (int)ntiles64;
     const int pairs_max = sm_count() / 2;
     const int npairs = ntiles < pairs_max ? ntiles : pairs_max;
-    gemm_bf16_pair_kernel<<<(unsigned)(2 * npairs), GB_THREADS, GP_SMEM, stream>>>(ma, mw, out, (int)m, (int)n, (int)k,
-                                                                                     ntm, ntiles);
+    gemm_bf16_pair_kernel<NB><<<(unsigned)(2 * npairs), GB_THREADS, smem, stream>>>(ma, mw, out, (int)m, (int)n, (int)k,
+                                                                                   ntm, ntiles);
     return check_launch(who);
+}
+
+// Both forms run a tile near the tensor pipe's rate, so the time is about rounds of tiles x
+// tile width: the 512-wide form where its rounds x 2 do not exceed the 256-wide form's rounds
+// (n = 16384: m = 512 and 4096 take it, m = 2048, 4 rounds against 7, does not).
+static int launch_pair(const uint16_t* a, const uint16_t* w, uint16_t* out, uint32_t m, uint32_t n, uint32_t k,
+                       cudaStream_t stream, int dev, const char* who) {
+    const uint64_t ntm = (m + 2 * GP_BM - 1) / (2 * GP_BM), pairs = (uint64_t)(sm_count() / 2);
+    auto rounds = [&](uint64_t bn) { return (ntm * ((n + bn - 1) / bn) + pairs - 1) / pairs; };
+    if (2 * rounds(2 * GP_BN) <= rounds(GP_BN)) return launch_pair_nb<2>(a, w, out, m, n, k, stream, dev, who);
+    return launch_pair_nb<1>(a, w, out, m, n, k, stream, dev, who);
 }
 
 extern "C" int dense_gemm_bf16(const uint16_t* a, const uint16_t* w, uint16_t* out, uint32_t m, uint32_t n,

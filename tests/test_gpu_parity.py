@@ -516,11 +516,14 @@ def test_dense_gemm_bf16_small(B, m, n, k):
     check_bf16_vs_f64(y, O.gemm_bf16(a, w), "dense gemm m=%d n=%d k=%d" % (m, n, k))
 
 
-@pytest.mark.parametrize("m,n,k", [(300, 20000, 128), (129, 39000, 64)])
+@pytest.mark.parametrize("m,n,k", [(300, 20000, 128), (129, 39000, 64), (300, 19000, 128), (520, 36000, 64)])
 def test_dense_gemm_bf16_persistent(B, m, n, k):
-    """More output tiles than SMs, so every CTA walks several tiles through both tensor-memory
-    accumulators (237 and 306 tiles of 128 x 256), with ragged last m and n tiles; every
-    element against the oracle."""
+    """More output tiles than SMs, so every CTA (pair) walks several tiles through its
+    tensor-memory accumulators, with ragged last m and n tiles; every element against the
+    oracle.  (300, 20000) and (129, 39000) take the 256 x 256 pair tiles (three rounds, two
+    accumulator buffers), (300, 19000) and (520, 36000) the 256 x 512 pair tiles (one and three
+    rounds through the one 512-column accumulator; in the last tile of n = 19000 the second
+    MMA's weight rows lie wholly past n)."""
     g = synth._gen(1400 + m + n + k)
     a = synth.activations(g, m, k)
     w = synth.dense_weight(g, n, k)
