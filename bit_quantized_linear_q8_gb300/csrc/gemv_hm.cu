@@ -424,9 +424,10 @@ __global__ void __launch_bounds__(HM_THREADS, 1)
     // row v / kv is a multiply-high by ceil(2^32 / kv): exact while v (ceil(2^32 / kv) kv -
     // 2^32) < 2^32, i.e. for every v < 8 kv when kv < 23170 (the host keeps k below that).
     // vectors of 8 values per thread and batch; the long-row (HPC = 4) form holds 2 * 17408
-    // values in one batch at M = 2, so that they are loaded once (at M = 3 a batch of 13
-    // vectors measured slower than two batches of 8)
-    constexpr int XV = HPC == 4 && M == 2 ? 9 : 8;
+    // values in one batch at M = 2, and the single-weight form at M >= 7 holds M * 5120, so that
+    // they are loaded once (m = 8, k = 5120: 15.9 -> 14.9 us; at M = 3 a batch of 13 vectors
+    // measured slower than two batches of 8, and the dual form at M = 8 did not gain)
+    constexpr int XV = HPC == 4 && M == 2 ? 9 : (HPC == 2 && M >= 7 && !DUAL ? 10 : 8);
     constexpr int NCT = HM_CWARPS * 32;
     const int kv = k >> 3;     // 8-value vectors per row
     const int tv = M * kv;     // vectors of x
